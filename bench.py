@@ -1,0 +1,424 @@
+"""Benchmark: one packed paged-KV attention tick (append + attention) per step.
+
+Default workload: the mixed tick with the Qwen3-4B attention shape (32 query
+heads, 8 KV heads, head_dim 128, bf16, 256-token pages): 96 decode tokens with
+contexts U[256, 4096] plus two 2048-token prefill chunks after cached prefixes of
+0 and 3072 tokens, 4192 packed rows, every row's K/V appended first. A step is
+the whole device path of one attention layer of that tick: kv_append, then
+paged_attention (work plan, prefill-chunk kernel, decode rows, split combine).
+
+Prints one JSON line. `value` is tokens/s (packed rows per second, whole job),
+timed with CUDA events per step on the launching stream, with the L2 flushed
+(a 512 MB write) between steps outside the timed events. `e2e` is the same
+metric through the public calls with host buffers: per step the host packs the
+tick, copies its inputs from pinned memory, runs the calls, and reads the
+outputs back. `--impl reference` times the CPU oracle on a bounded sample of the
+same workload instead.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from paged_kv_attention_mapping_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged-attn decode HBM GB/s (vs ~8 TB/s) and mixed-tick tokens/s on 1 GB300"
+L2_FLUSH_BYTES = 512 << 20
+
+DESCRIPTIONS = {
+    "tiny_decode": "4 decode seqs, kv {17,64,100,255}, 8/2 heads, d64, page 16",
+    "tinyllama_decode": "64 decode seqs, kv U[128,2048], 32/4 heads, d64, fp16, page 16, 64-token append",
+    "qwen3_decode": "128 decode seqs, kv U[512,8192], 32/8 heads, d128, bf16, page 256, 128-token append",
+    "mixed_tick": ("Qwen3-4B attention shape (32/8 heads, d128, bf16, page 256): 96 decode tokens kv U[256,4096] "
+                   "+ prefill chunks 2048@prefix0 and 2048@prefix3072, 4192 packed rows, appended first"),
+    "shared_prefix_long": "16 decode seqs of kv 32768, 16 shared prefix pages, Qwen3-4B shape, bf16, split-KV",
+}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work of the tick (bytes and flops a perfect kernel must move/do)
+
+def tick_work(w):
+    s = w.shape
+    elt = s.elt_bytes
+    row_bytes = s.num_kv_heads * s.head_dim * elt        # one token's K (or V) for all KV heads
+    dec_rows = [r for r in w.requests if r.q_len == 1]
+    chunk = [r for r in w.requests if r.q_len > 1]
+    decode_kv = sum(2 * r.kv_len * row_bytes for r in dec_rows)
+    decode_qo = sum(2 * s.num_q_heads * s.head_dim * elt + 4 * s.num_q_heads for r in dec_rows)
+    decode_pt = sum(4 * len(r.pages) for r in dec_rows)
+    pairs = sum(r.q_len * (r.kv_len - r.q_len) + r.q_len * (r.q_len + 1) // 2 for r in chunk)
+    prefill_flops = 4 * s.head_dim * s.num_q_heads * pairs
+    prefill_bytes = sum(2 * r.kv_len * row_bytes + 2 * r.q_len * s.num_q_heads * s.head_dim * elt for r in chunk)
+    append_bytes = 2 * 2 * w.total_q * row_bytes         # K and V: read the rows, write the slots
+    return dict(decode_bytes=decode_kv + decode_qo + decode_pt, decode_kv_bytes=decode_kv,
+                prefill_flops=prefill_flops, prefill_bytes=prefill_bytes, append_bytes=append_bytes)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample (the reported baseline)
+
+def oracle_sample(w, seconds=12.0, seed=0):
+    """Time the oracle (pack, append, attend) on a sample of the tick's rows and
+    scale to the whole tick: returns (tokens/s, description, threads)."""
+    import oracle
+    vals_rng = np.random.default_rng([w.seed, 7])
+    s = w.shape
+    ql = [r.q_len for r in w.requests]
+    kl = [r.kv_len for r in w.requests]
+    pg = [r.pages for r in w.requests]
+    t0 = time.perf_counter()
+    p = oracle.pack_tick(ql, kl, pg, s.page_size)
+    t_pack = time.perf_counter() - t0
+    rng = np.random.default_rng(seed)
+    cu = p["cu_seqlens_q"]
+    B = len(ql)
+    kinds = {"decode": [b for b in range(B) if cu[b + 1] - cu[b] == 1],
+             "chunk": [b for b in range(B) if cu[b + 1] - cu[b] > 1]}
+    rows_total = {k: int(sum(cu[b + 1] - cu[b] for b in v)) for k, v in kinds.items()}
+    spent = {"decode": 0.0, "chunk": 0.0}
+    done = {"decode": 0, "chunk": 0}
+    deadline = time.perf_counter() + seconds
+    while time.perf_counter() < deadline:
+        kind = min((k for k in kinds if kinds[k]), key=lambda k: spent[k] / max(rows_total[k], 1) if done[k] else -1)
+        b = int(rng.choice(kinds[kind]))
+        r = w.requests[p["order"][b]]
+        n_rows = r.q_len if kind == "decode" else min(16, r.q_len)
+        # this sequence's pages, a fresh draw of its values, its new tokens
+        pages = list(range(len(r.pages)))
+        kc = W.round_to_dtype(vals_rng.standard_normal((len(pages), s.page_size, s.num_kv_heads, s.head_dim),
+                                                       dtype=np.float32), s.dtype)
+        vc = W.round_to_dtype(vals_rng.standard_normal(kc.shape, dtype=np.float32), s.dtype)
+        qn = W.round_to_dtype(vals_rng.standard_normal((r.q_len, s.num_q_heads, s.head_dim), dtype=np.float32),
+                              s.dtype)
+        kn = W.round_to_dtype(vals_rng.standard_normal((r.q_len, s.num_kv_heads, s.head_dim), dtype=np.float32),
+                              s.dtype)
+        vn = W.round_to_dtype(vals_rng.standard_normal(kn.shape, dtype=np.float32), s.dtype)
+        t0 = time.perf_counter()
+        sp = oracle.pack_tick([r.q_len], [r.kv_len], [pages], s.page_size)
+        kc2, vc2 = oracle.kv_append(kc, vc, kn, vn, sp["slot_mapping"])
+        rows = sorted(rng.choice(r.q_len, size=n_rows, replace=False).tolist())
+        oracle.paged_attention(qn, sp["cu_seqlens_q"], sp["kv_lens"], sp["page_tables"], kc2, vc2, w.scale, rows=rows)
+        spent[kind] += time.perf_counter() - t0
+        done[kind] += n_rows
+    est = t_pack + sum(spent[k] / done[k] * rows_total[k] for k in kinds if rows_total[k])
+    tokens_s = w.total_q / est
+    desc = (f"oracle on {done['decode']} decode rows and {done['chunk']} chunk rows drawn from the tick "
+            f"({sum(spent.values()):.1f} s of CPU), scaled per row kind to all {w.total_q} rows")
+    threads = 1
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        threads = int(os.environ.get("OMP_NUM_THREADS", "0") or 0) or len(os.sched_getaffinity(0))
+    return tokens_s, desc, threads
+
+
+# ---------------------------------------------------------------------------
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = W.make_workload(args.workload)
+    per_step = []
+    desc = ""
+    threads = 1
+    total_budget = 20.0
+    steps = max(1, args.steps)
+    secs = max(1.0, total_budget / (steps + args.warmup))
+    for i in range(args.warmup + steps):
+        tok_s, desc, threads = oracle_sample(w, seconds=secs, seed=i)
+        if i >= args.warmup:
+            per_step.append(w.total_q / tok_s * 1000.0)
+    ms = statistics.mean(per_step)
+    value = w.total_q / (ms / 1000.0)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mixed_tick", choices=list(W.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.warmup < 3:
+        args.warmup = 3
+
+    import torch
+    world, rank, local = dist_setup(args.gpus)
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    from paged_kv_attention_mapping_gb300 import build as B
+    B.build()
+    from paged_kv_attention_mapping_gb300 import binding
+
+    w = W.make_workload(args.workload)
+    s = w.shape
+    ql = [r.q_len for r in w.requests]
+    kl = [r.kv_len for r in w.requests]
+    pg = [r.pages for r in w.requests]
+    packed = binding.pack_tick(ql, kl, pg, s.page_size, w.num_pages)
+    vals = W.device_values(w, dev)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    cu, kv, pt = i32(packed["cu_seqlens_q"]), i32(packed["kv_lens"]), i32(packed["page_tables"])
+    slots = i32(packed["slot_mapping"])
+    q, kn, vn, kc, vc = vals["q"], vals["k_new"], vals["v_new"], vals["k_cache"], vals["v_cache"]
+    T = w.total_q
+    out = torch.empty_like(q)
+    lse = torch.empty((T, s.num_q_heads), dtype=torch.float32, device=dev)
+    ws = binding.alloc_workspace(len(ql), T, s.num_q_heads, kc, w.max_kv_len)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        binding.kv_append(kn, vn, slots, kc, vc)
+        binding.paged_attention(q, cu, kv, pt, kc, vc, w.scale, w.max_kv_len, out=out, lse=lse, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # pass A: the headline number (no per-kernel events)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    binding.set_kernel_timing(False)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * T / (ms / 1000.0)
+
+    # pass B: per-kernel device time (events on the launch stream around each kernel)
+    binding.set_kernel_timing(True)
+    binding.kernel_times()
+    for _ in range(args.steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ktimes = binding.kernel_times()
+    binding.set_kernel_timing(False)
+    launches_per_step = sum(n for n, _ in ktimes.values()) / args.steps
+
+    # e2e: host buffers through the public calls
+    pin = lambda t: t.cpu().pin_memory()
+    h_q, h_k, h_v = pin(q), pin(kn), pin(vn)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
+    meta_bytes = 0
+
+    def e2e_step():
+        nonlocal meta_bytes
+        pk = binding.pack_tick(ql, kl, pg, s.page_size, w.num_pages)
+        h_meta = [torch.from_numpy(pk[k]).pin_memory() for k in ("cu_seqlens_q", "kv_lens", "page_tables",
+                                                                  "slot_mapping")]
+        d_meta = [m.to(dev, non_blocking=True) for m in h_meta]
+        meta_bytes = sum(m.numel() * m.element_size() for m in h_meta)
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        binding.kv_append(d_k, d_v, d_meta[3], kc, vc)
+        binding.paged_attention(d_q, d_meta[0], d_meta[1], d_meta[2], kc, vc, w.scale, w.max_kv_len, out=out,
+                                lse=lse, workspace=ws)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_step()
+        e2e_ms.append((time.perf_counter() - t0) * 1000.0)
+    e2e_avg = statistics.mean(e2e_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_avg], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_avg = float(t.item())
+    h2d = meta_bytes + sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v))
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+    if rank != 0:
+        return 0
+
+    peaks = load_peaks()
+    work = tick_work(w)
+    per_kernel = {k: {"launches": n, "avg_us": 1000.0 * t / n, "share": None} for k, (n, t) in ktimes.items()}
+    tot = sum(t for _, t in ktimes.values()) or 1.0
+    for k, (n, t) in ktimes.items():
+        per_kernel[k]["share"] = t / tot
+    dom = max(ktimes, key=lambda k: ktimes[k][1]) if ktimes else None
+    roof = None
+    if dom is not None:
+        avg_s = ktimes[dom][1] / ktimes[dom][0] / 1000.0
+        if dom == "prefill_tc":
+            ach = work["prefill_flops"] / avg_s / 1e12
+            roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": None,
+                    "algorithmic_per_launch": work["prefill_flops"]}
+        else:
+            nbytes = {"rows": work["decode_bytes"], "decode_tc": work["decode_bytes"],
+                      "kv_append": work["append_bytes"]}.get(dom, work["decode_bytes"])
+            ach = nbytes / avg_s / 1e9
+            roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": ach / peaks["hbm_gbs"], "traffic": None, "algorithmic_per_launch": nbytes}
+        roof["peak_source"] = peaks["source"]
+    decode_k = "rows" if "rows" in ktimes else None
+    decode_gbs = None
+    if decode_k and work["decode_bytes"]:
+        decode_gbs = work["decode_bytes"] / (ktimes[decode_k][1] / ktimes[decode_k][0] / 1000.0) / 1e9
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        tok_s, desc, threads = oracle_sample(w, seconds=args.cpu_seconds)
+        cpu = {"value": tok_s, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": s.dtype, "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+                   "tokens_per_step": T, "l2": "flushed between steps (512 MB write, outside the step events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "roofline": roof,
+        "decode_hbm_gbs": decode_gbs,
+        "kernels": per_kernel,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * T / (e2e_avg / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_avg},
+        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,216 @@
+/*
+ * pagedkv.h — C ABI of libpagedkv: attention over a paged KV cache for one
+ * packed, continuously batched tick of decode tokens and chunked-prefill
+ * tokens with grouped-query heads, on an NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the serving pages' description of the problem:
+ *  - the KV cache is a fixed pool of fixed-size pages shared by all sequences,
+ *    one tensor per layer for K and one for V, each laid out
+ *    [num_pages, page_size, num_kv_heads, head_dim] (llm-serving-engine README,
+ *    component table "KV Cache" row and "KV cache memory layout" figure;
+ *    Helios README, "Paged attention": a fixed pool of 256-token pages);
+ *  - each sequence owns a page table that maps its positions to pages
+ *    (mini-vLLM, "Paged KV-cache"; Helios README, "Paged attention");
+ *  - new tokens' K/V are written into their slots first, then attention reads
+ *    K/V through the page tables, never copying them into dense per-sequence
+ *    buffers (Helios README, "Paged attention" and its closing remark on
+ *    causal paged attention on NVIDIA GPUs; Helios blog, "Prefill vs Decode");
+ *  - decode tokens and prefill chunks run in one packed pass with independent
+ *    positions and page tables, decode tokens first (Helios README,
+ *    "Continuous batching"; Helios blog, "Continuous batching").
+ *
+ * Conventions shared by every call:
+ *  - Ownership: the caller allocates and owns every buffer, host or device,
+ *    including the attention workspace. The library allocates no device memory
+ *    and keeps no per-call state. It does hold, per process, a device status
+ *    word (see pkv_get_device_status) and, when enabled, CUDA events for
+ *    kernel timing.
+ *  - Asynchrony: device calls are enqueued on `stream` (a cudaStream_t; NULL =
+ *    the legacy default stream) and return before the work runs. Outputs are
+ *    valid once the stream has been synchronised.
+ *  - Errors: every call returns PKV_OK (0) or a negative PKV_E_* code. Host
+ *    checks run before anything is enqueued; on an error nothing is launched.
+ *    Data-dependent checks that only the device can make (a slot or page id
+ *    outside the pool, a kv_len longer than its page table) set bits of the
+ *    device status word and skip the offending row; nothing traps or aborts.
+ *  - Dtypes: K, V, Q and the attention output share one dtype (PKV_F32,
+ *    PKV_F16 or PKV_BF16); accumulation is fp32; lse is fp32.
+ */
+#ifndef PAGEDKV_H_
+#define PAGEDKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pkv_stream_t; /* same handle as cudaStream_t */
+
+typedef enum {
+  PKV_F32 = 0,
+  PKV_F16 = 1,
+  PKV_BF16 = 2
+} pkv_dtype;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_E_NULL = -1,      /* a required pointer is NULL */
+  PKV_E_DTYPE = -2,     /* unknown dtype */
+  PKV_E_SHAPE = -3,     /* a size is out of range, Hq % Hkv != 0, or head_dim unsupported */
+  PKV_E_LENGTHS = -4,   /* q/kv lengths break 0 <= q_len <= kv_len (host-checked calls) */
+  PKV_E_PAGES = -5,     /* a page id outside the pool, or too few pages for a length */
+  PKV_E_WORKSPACE = -6, /* workspace smaller than pkv_paged_attention_workspace_size */
+  PKV_E_ALIGN = -7,     /* a pointer is not 16-byte aligned */
+  PKV_E_CUDA = -8,      /* a CUDA runtime call or launch failed */
+  PKV_E_DEVICE = -9,    /* the current device is not an sm_103 GPU */
+  PKV_E_CAPACITY = -10  /* an output buffer is too small (host-checked calls) */
+} pkv_status;
+
+/* Bits of the device status word. */
+#define PKV_DEV_BAD_SLOT 0x1    /* kv_append: slot >= num_pages * page_size; that row skipped */
+#define PKV_DEV_BAD_LENGTHS 0x2 /* attention: q_len < 0, kv_len < q_len, kv_len < 1 with rows,
+                                   kv_len > max_kv_len or > max_pages_per_seq * page_size;
+                                   that sequence's rows are skipped */
+#define PKV_DEV_BAD_PAGE 0x4    /* attention: a page id needed by a row is outside the pool;
+                                   that row's output is left unwritten */
+
+/* One layer's K (or V) page pool: contiguous
+ * [num_pages, page_size, num_kv_heads, head_dim] of `dtype`. */
+typedef struct {
+  int32_t num_pages;
+  int32_t page_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t dtype; /* pkv_dtype */
+} pkv_cache_desc;
+
+/* ---------------------------------------------------------------------------
+ * pkv_pack_tick — host-side packing of one tick (no device work).
+ *
+ * Puts decode sequences (q_len == 1) first and then the others, each group in
+ * arrival order (Helios README, "Continuous batching": every tick first takes
+ * one token per decoding request, then spends the rest of the budget on
+ * prompts; both run in one packed forward), and builds the packed metadata.
+ *
+ * In (host pointers, num_seqs entries unless stated):
+ *   q_lens[i]        tokens sequence i adds this tick (0 = idle, 1 = decode, >1 = chunk)
+ *   kv_lens[i]       context length after this tick's tokens are written
+ *   page_offsets     [num_seqs + 1], CSR offsets into page_ids
+ *   page_ids         physical pages of sequence i in logical order:
+ *                    page_ids[page_offsets[i] .. page_offsets[i+1])
+ *   page_size, num_pages, max_pages_per_seq (width of the output table)
+ *   slot_capacity    length of the slot_mapping buffer
+ * Out (host pointers, caller-allocated):
+ *   order[num_seqs]                   arrival index of the i-th packed sequence
+ *   cu_seqlens_q[num_seqs + 1]        row offsets of the packed sequences
+ *   kv_lens_out[num_seqs]             kv_len of the i-th packed sequence
+ *   page_tables[num_seqs * max_pages_per_seq]  row-major, unused entries -1
+ *   slot_mapping[total_q]             page * page_size + offset of each packed
+ *                                     row's new token (its position is
+ *                                     kv_len - q_len + i for chunk row i)
+ *   total_q_out                       number of packed rows
+ * Errors: PKV_E_NULL, PKV_E_SHAPE (num_seqs < 0, page_size < 1, num_pages < 1,
+ * max_pages_per_seq < 1), PKV_E_LENGTHS (q_len < 0, kv_len < q_len, kv_len < 1
+ * with q_len > 0), PKV_E_PAGES (page id outside [0, num_pages), fewer pages
+ * than ceil(kv_len / page_size), more pages than max_pages_per_seq),
+ * PKV_E_CAPACITY (total_q > slot_capacity). Outputs are unspecified on error.
+ */
+int pkv_pack_tick(int32_t num_seqs, const int32_t* q_lens, const int32_t* kv_lens,
+                  const int32_t* page_offsets, const int32_t* page_ids,
+                  int32_t page_size, int32_t num_pages, int32_t max_pages_per_seq,
+                  int32_t slot_capacity,
+                  int32_t* order, int32_t* cu_seqlens_q, int32_t* kv_lens_out,
+                  int32_t* page_tables, int64_t* slot_mapping, int32_t* total_q_out);
+
+/* ---------------------------------------------------------------------------
+ * pkv_kv_append — write each new token's K and V rows into its slot
+ * (Helios blog, "Prefill vs Decode": a decode step writes its new token's
+ * slot; Helios README, "Paged attention": decode stores straight into the
+ * shared pool; llm-serving-engine README, engine step trace: a prefill chunk
+ * stores its K/V starting at the chunk's first position).
+ *
+ *   k, v          device, [num_tokens, num_kv_heads, head_dim], contiguous, cache dtype
+ *   slot_mapping  device, int64 [num_tokens]; row t goes to page slot / page_size,
+ *                 offset slot % page_size; a negative slot skips the row
+ *   k_cache, v_cache  device, the pools described by `cache`
+ * Bit-exact copy. Duplicate non-negative slots in one call are a caller error
+ * (which row lands is unspecified). A slot >= num_pages * page_size sets
+ * PKV_DEV_BAD_SLOT and skips the row. num_tokens == 0 is a no-op.
+ * Errors: PKV_E_NULL, PKV_E_DTYPE, PKV_E_SHAPE, PKV_E_ALIGN (k, v, caches must
+ * be 16-byte aligned), PKV_E_CUDA.
+ */
+int pkv_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int32_t num_tokens,
+                  void* k_cache, void* v_cache, const pkv_cache_desc* cache, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * pkv_paged_attention_workspace_size — bytes of device workspace that
+ * pkv_paged_attention needs for these sizes (0 on invalid sizes).
+ * The workspace holds the device-side work plan and the split-KV partial
+ * results; its contents need no initialisation and are not preserved.
+ */
+size_t pkv_paged_attention_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                                          const pkv_cache_desc* cache, int32_t max_kv_len);
+
+/* ---------------------------------------------------------------------------
+ * pkv_paged_attention — attention of every packed query row over its
+ * sequence's pages (Helios blog, "torch.sdpa and Flash Attention":
+ * softmax(Q K^T * scale) V with grouped-query heads sharing KV heads;
+ * llm-serving-engine README, engine step trace: a prefill chunk after cached
+ * K/V uses a rectangular causal mask, a decode row attends the full context).
+ *
+ *   q             device, [total_q, num_q_heads, head_dim], cache dtype, contiguous
+ *   cu_seqlens_q  device, int32 [num_seqs + 1]; cu[0] = 0, non-decreasing, cu[num_seqs] = total_q
+ *   kv_lens       device, int32 [num_seqs]; context length INCLUDING this tick's
+ *                 tokens (append first, then attend)
+ *   page_tables   device, int32 [num_seqs, max_pages_per_seq], row-major
+ *   max_kv_len    host upper bound on every kv_lens entry (sizes the work plan)
+ *   scale         multiplies q.k before the softmax
+ *   out           device, [total_q, num_q_heads, head_dim], cache dtype
+ *   lse           device, fp32 [total_q, num_q_heads], natural log of
+ *                 sum_j exp(scale * q.k_j); may be NULL
+ *   workspace     device, >= pkv_paged_attention_workspace_size(...) bytes, 256-byte aligned
+ * Row i of sequence b (q_len = cu[b+1] - cu[b], kv_len = kv_lens[b]) attends
+ * keys 0 .. kv_len - q_len + i. q head h reads KV head h / (num_q_heads /
+ * num_kv_heads). Page-table entries past ceil(kv_len / page_size) and slots at
+ * positions >= kv_len are never read and may hold anything (NaN, -1).
+ * Rows of sequences with bad lengths or pages (see the device status bits)
+ * are skipped.
+ * Errors: PKV_E_NULL, PKV_E_DTYPE, PKV_E_SHAPE (num_q_heads % num_kv_heads != 0,
+ * head_dim not 64 or 128, sizes < 0), PKV_E_ALIGN, PKV_E_WORKSPACE,
+ * PKV_E_DEVICE, PKV_E_CUDA.
+ */
+int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                        const int32_t* page_tables, int32_t num_seqs, int32_t total_q,
+                        int32_t num_q_heads, int32_t max_pages_per_seq, int32_t max_kv_len,
+                        const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                        float scale, void* out, float* lse,
+                        void* workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Status and instrumentation. */
+
+/* Human-readable text for a pkv_status code (static storage). */
+const char* pkv_status_string(int status);
+
+/* Waits for `stream`, then returns in *code the OR of the PKV_DEV_* bits set
+ * on the current device since the last call, and clears them. */
+int pkv_get_device_status(int32_t* code, pkv_stream_t stream);
+
+/* Kernel timing: when enabled (1), every kernel the library launches is
+ * bracketed by CUDA events on its launch stream; pkv_kernel_times waits for
+ * the recorded work and returns, per kernel name, the number of launches and
+ * the summed device time, then clears the record. Disabled (0) by default. */
+int pkv_set_kernel_timing(int enable);
+/* Fills up to `max` entries; returns the number of kernels recorded (>= 0) or
+ * a negative pkv_status. names[i] points at static storage. */
+int pkv_kernel_times(const char** names, int32_t* launches, double* total_ms, int32_t max);
+
+/* Library version string. */
+const char* pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGEDKV_H_ */

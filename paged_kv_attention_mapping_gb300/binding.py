@@ -1,0 +1,241 @@
+"""Thin ctypes binding of libpagedkv (declared in include/pagedkv.h).
+
+Argument marshalling only: torch tensors become device pointers and the
+current torch stream becomes the cudaStream_t; every step of the computation
+runs in the library's kernels. There is no fallback: if the library is missing
+or cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+
+PKV_F32, PKV_F16, PKV_BF16 = 0, 1, 2
+DEV_BAD_SLOT, DEV_BAD_LENGTHS, DEV_BAD_PAGE = 0x1, 0x2, 0x4
+
+EXPORTED = (
+    "pkv_pack_tick",
+    "pkv_kv_append",
+    "pkv_paged_attention_workspace_size",
+    "pkv_paged_attention",
+    "pkv_status_string",
+    "pkv_get_device_status",
+    "pkv_set_kernel_timing",
+    "pkv_kernel_times",
+    "pkv_version",
+)
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libpagedkv.so (built by paged_kv_attention_mapping_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libpagedkv.so is not built ({LIB_PATH}); run "
+                           "`python -c 'import __graft_entry__ as g; g.build()'` first")
+    L = ctypes.CDLL(LIB_PATH)
+    i32, i64, vp, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+    P32, P64 = ctypes.POINTER(i32), ctypes.POINTER(i64)
+    L.pkv_pack_tick.argtypes = [i32, P32, P32, P32, P32, i32, i32, i32, i32, P32, P32, P32, P32, P64, P32]
+    L.pkv_pack_tick.restype = ctypes.c_int
+    L.pkv_kv_append.argtypes = [vp, vp, vp, i32, vp, vp, ctypes.POINTER(CacheDesc), vp]
+    L.pkv_kv_append.restype = ctypes.c_int
+    L.pkv_paged_attention_workspace_size.argtypes = [i32, i32, i32, ctypes.POINTER(CacheDesc), i32]
+    L.pkv_paged_attention_workspace_size.restype = sz
+    L.pkv_paged_attention.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp,
+                                      ctypes.POINTER(CacheDesc), ctypes.c_float, vp, vp, vp, sz, vp]
+    L.pkv_paged_attention.restype = ctypes.c_int
+    L.pkv_status_string.argtypes = [ctypes.c_int]
+    L.pkv_status_string.restype = ctypes.c_char_p
+    L.pkv_get_device_status.argtypes = [P32, vp]
+    L.pkv_get_device_status.restype = ctypes.c_int
+    L.pkv_set_kernel_timing.argtypes = [ctypes.c_int]
+    L.pkv_set_kernel_timing.restype = ctypes.c_int
+    L.pkv_kernel_times.argtypes = [ctypes.POINTER(ctypes.c_char_p), P32, ctypes.POINTER(ctypes.c_double), i32]
+    L.pkv_kernel_times.restype = ctypes.c_int
+    L.pkv_version.argtypes = []
+    L.pkv_version.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().pkv_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return lib().pkv_version().decode()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise PagedKVError(status, where)
+
+
+# ---------------------------------------------------------------------------
+# host packing
+
+def pack_tick(q_lens: Sequence[int], kv_lens: Sequence[int], pages: Sequence[Sequence[int]], page_size: int,
+              num_pages: int, max_pages_per_seq: Optional[int] = None):
+    """Host packing of one tick (pkv_pack_tick). Returns numpy arrays:
+    order, cu_seqlens_q, kv_lens, page_tables [B, W] (-1 padded), slot_mapping."""
+    B = len(q_lens)
+    W = int(max_pages_per_seq if max_pages_per_seq is not None else max((len(p) for p in pages), default=1))
+    W = max(W, 1)
+    ql = np.ascontiguousarray(q_lens, dtype=np.int32)
+    kl = np.ascontiguousarray(kv_lens, dtype=np.int32)
+    offs = np.zeros(B + 1, dtype=np.int32)
+    offs[1:] = np.cumsum([len(p) for p in pages]) if B else []
+    ids = np.ascontiguousarray(np.concatenate([np.asarray(p, dtype=np.int32) for p in pages])
+                               if B and offs[-1] > 0 else np.zeros(1, dtype=np.int32), dtype=np.int32)
+    cap = int(max(int(ql.clip(min=0).sum()), 1))
+    order = np.zeros(max(B, 1), dtype=np.int32)
+    cu = np.zeros(B + 1, dtype=np.int32)
+    kv_out = np.zeros(max(B, 1), dtype=np.int32)
+    tables = np.zeros((max(B, 1), W), dtype=np.int32)
+    slots = np.zeros(cap, dtype=np.int64)
+    total = np.zeros(1, dtype=np.int32)
+    P32 = ctypes.POINTER(ctypes.c_int32)
+
+    def p32(a):
+        return a.ctypes.data_as(P32)
+
+    st = lib().pkv_pack_tick(B, p32(ql) if B else None, p32(kl) if B else None, p32(offs), p32(ids),
+                             int(page_size), int(num_pages), W, cap, p32(order), p32(cu), p32(kv_out),
+                             p32(tables), slots.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), p32(total))
+    _check(st, "pkv_pack_tick")
+    T = int(total[0])
+    return dict(order=order[:B], cu_seqlens_q=cu, kv_lens=kv_out[:B], page_tables=tables[:B],
+                slot_mapping=slots[:T])
+
+
+# ---------------------------------------------------------------------------
+# device calls (torch tensors)
+
+def _dtype_code(t) -> int:
+    import torch
+    m = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
+    if t.dtype not in m:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return m[t.dtype]
+
+
+def cache_desc(k_cache) -> CacheDesc:
+    if k_cache.dim() != 4 or not k_cache.is_contiguous():
+        raise ValueError("cache must be a contiguous [num_pages, page_size, num_kv_heads, head_dim] tensor")
+    N, P, H, D = k_cache.shape
+    return CacheDesc(N, P, H, D, _dtype_code(k_cache))
+
+
+def _stream_ptr(stream=None) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+def kv_append(k, v, slot_mapping, k_cache, v_cache, stream=None):
+    """Write new tokens' K/V rows into their slots (pkv_kv_append)."""
+    for t in (k, v, slot_mapping, k_cache, v_cache):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("kv_append needs contiguous CUDA tensors")
+    import torch
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    desc = cache_desc(k_cache)
+    st = lib().pkv_kv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), int(k.shape[0]), _ptr(k_cache), _ptr(v_cache),
+                             ctypes.byref(desc), _stream_ptr(stream))
+    _check(st, "pkv_kv_append")
+
+
+def workspace_size(num_seqs: int, total_q: int, num_q_heads: int, k_cache, max_kv_len: int) -> int:
+    desc = cache_desc(k_cache)
+    n = lib().pkv_paged_attention_workspace_size(int(num_seqs), int(total_q), int(num_q_heads), ctypes.byref(desc),
+                                                 int(max_kv_len))
+    if n == 0:
+        raise PagedKVError(-3, "pkv_paged_attention_workspace_size")
+    return int(n)
+
+
+def alloc_workspace(num_seqs, total_q, num_q_heads, k_cache, max_kv_len):
+    import torch
+    n = workspace_size(num_seqs, total_q, num_q_heads, k_cache, max_kv_len)
+    return torch.empty(n, dtype=torch.uint8, device=k_cache.device)
+
+
+def paged_attention(q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_cache, scale: float, max_kv_len: int,
+                    out=None, lse=None, workspace=None, want_lse: bool = True, stream=None):
+    """Attention of packed query rows over their pages (pkv_paged_attention).
+
+    q [T, Hq, d] (cache dtype); cu_seqlens_q int32 [B+1]; kv_lens int32 [B];
+    page_tables int32 [B, W]; caches [N, P, Hkv, d]. Returns (out, lse)."""
+    import torch
+    T, Hq, D = q.shape
+    B = int(cu_seqlens_q.shape[0]) - 1
+    for t in (q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_cache):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("paged_attention needs contiguous CUDA tensors")
+    for t in (cu_seqlens_q, kv_lens, page_tables):
+        if t.dtype != torch.int32:
+            raise TypeError("index tensors must be int32")
+    if q.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
+        raise TypeError("q, k_cache and v_cache must share one dtype")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(B, T, Hq, k_cache, max_kv_len)
+    desc = cache_desc(k_cache)
+    st = lib().pkv_paged_attention(_ptr(q), _ptr(cu_seqlens_q), _ptr(kv_lens), _ptr(page_tables), B, int(T), int(Hq),
+                                   int(page_tables.shape[1]), int(max_kv_len), _ptr(k_cache), _ptr(v_cache),
+                                   ctypes.byref(desc), ctypes.c_float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                   int(workspace.numel()), _stream_ptr(stream))
+    _check(st, "pkv_paged_attention")
+    return out, lse
+
+
+def device_status(stream=None) -> int:
+    """OR of the device status bits since the last call (then cleared)."""
+    code = ctypes.c_int32(0)
+    _check(lib().pkv_get_device_status(ctypes.byref(code), _stream_ptr(stream)), "pkv_get_device_status")
+    return int(code.value)
+
+
+def set_kernel_timing(enable: bool):
+    _check(lib().pkv_set_kernel_timing(1 if enable else 0), "pkv_set_kernel_timing")
+
+
+def kernel_times(max_kernels: int = 32):
+    """{kernel name: (launches, total ms)} recorded since the last call."""
+    names = (ctypes.c_char_p * max_kernels)()
+    launches = (ctypes.c_int32 * max_kernels)()
+    total = (ctypes.c_double * max_kernels)()
+    n = lib().pkv_kernel_times(names, launches, total, max_kernels)
+    if n < 0:
+        raise PagedKVError(n, "pkv_kernel_times")
+    return {names[i].decode(): (int(launches[i]), float(total[i])) for i in range(n)}

@@ -1,0 +1,295 @@
+// C-ABI entry points of libpagedkv: host-side checks, the work plan, launches
+// on the caller's stream, the device status word and kernel timing.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "pagedkv.h"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+// ---------------------------------------------------------------------------
+// per-device facts and the device status word
+
+__device__ int32_t g_device_status;
+
+struct DeviceFacts {
+  bool ready = false;
+  int ok = 0;  // 1 = sm_103
+  int num_sms = 0;
+  int32_t* status = nullptr;
+};
+static std::mutex g_dev_mu;
+static DeviceFacts g_dev[64];
+
+static const DeviceFacts* device_facts() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceFacts& f = g_dev[dev];
+  if (!f.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return nullptr;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return nullptr;
+    if (cudaDeviceGetAttribute(&f.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    f.status = (int32_t*)p;
+    f.ok = (major == 10 && minor == 3) ? 1 : 0;
+    f.ready = true;
+  }
+  return &f;
+}
+
+int32_t* device_status_ptr() {
+  const DeviceFacts* f = device_facts();
+  return f ? f->status : nullptr;
+}
+
+// ---------------------------------------------------------------------------
+// kernel timing
+
+struct TimingRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+static std::mutex g_t_mu;
+static bool g_timing = false;
+static std::vector<TimingRec> g_recs;
+static std::vector<cudaEvent_t> g_free_events;
+
+static cudaEvent_t take_event() {
+  if (!g_free_events.empty()) {
+    cudaEvent_t e = g_free_events.back();
+    g_free_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+KernelTimer::KernelTimer(const char* name, cudaStream_t s) : name_(name), s_(s), slot_(-1) {
+  std::lock_guard<std::mutex> lk(g_t_mu);
+  if (!g_timing) return;
+  TimingRec r{name, take_event(), take_event()};
+  if (!r.a || !r.b) return;
+  cudaEventRecord(r.a, s);
+  g_recs.push_back(r);
+  slot_ = (int)g_recs.size() - 1;
+}
+
+KernelTimer::~KernelTimer() {
+  if (slot_ < 0) return;
+  std::lock_guard<std::mutex> lk(g_t_mu);
+  if (slot_ < (int)g_recs.size()) cudaEventRecord(g_recs[slot_].b, s_);
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+// ---------------------------------------------------------------------------
+// C ABI
+
+extern "C" const char* pkv_version(void) { return "pagedkv 0.1 (sm_103a)"; }
+
+extern "C" const char* pkv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_E_NULL: return "a required pointer is NULL";
+    case PKV_E_DTYPE: return "unknown dtype";
+    case PKV_E_SHAPE: return "unsupported or inconsistent sizes";
+    case PKV_E_LENGTHS: return "q/kv lengths break 0 <= q_len <= kv_len";
+    case PKV_E_PAGES: return "page id outside the pool or too few pages";
+    case PKV_E_WORKSPACE: return "workspace too small or misaligned";
+    case PKV_E_ALIGN: return "pointer not 16-byte aligned";
+    case PKV_E_CUDA: return "CUDA runtime error";
+    case PKV_E_DEVICE: return "current device is not an sm_103 GPU";
+    case PKV_E_CAPACITY: return "output buffer too small";
+    default: return "unknown status";
+  }
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static int check_cache(const pkv_cache_desc* c) {
+  if (!c) return PKV_E_NULL;
+  if (c->dtype < PKV_F32 || c->dtype > PKV_BF16) return PKV_E_DTYPE;
+  if (c->num_pages < 1 || c->page_size < 1 || c->num_kv_heads < 1 || c->head_dim < 1) return PKV_E_SHAPE;
+  const int elt = c->dtype == PKV_F32 ? 4 : 2;
+  if (((int64_t)c->num_kv_heads * c->head_dim * elt) % 16 != 0) return PKV_E_SHAPE;
+  if ((int64_t)c->num_pages * c->page_size > INT32_MAX) return PKV_E_SHAPE;
+  return PKV_OK;
+}
+
+extern "C" int pkv_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int32_t num_tokens,
+                             void* k_cache, void* v_cache, const pkv_cache_desc* cache, pkv_stream_t stream) {
+  int st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_E_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_E_NULL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) || ((uintptr_t)slot_mapping & 7u))
+    return PKV_E_ALIGN;
+  const DeviceFacts* f = device_facts();
+  if (!f) return PKV_E_CUDA;
+  if (!f->ok) return PKV_E_DEVICE;
+  cudaError_t e = launch_append(k, v, slot_mapping, num_tokens, k_cache, v_cache, *cache, (cudaStream_t)stream);
+  return e == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+}
+
+static bool head_dim_supported(int d) { return d == 64 || d == 128; }
+static bool group_supported(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16; }
+
+extern "C" size_t pkv_paged_attention_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                                                     const pkv_cache_desc* cache, int32_t max_kv_len) {
+  if (check_cache(cache) != PKV_OK || num_seqs < 0 || total_q < 0 || num_q_heads < 1 || max_kv_len < 0) return 0;
+  if (num_q_heads % cache->num_kv_heads != 0) return 0;
+  return plan_layout(num_seqs, total_q, num_q_heads, cache->num_kv_heads, cache->head_dim, max_kv_len).total;
+}
+
+// Sequences whose chunk has at least this many rows run on the tensor-core
+// prefill kernel (when the shape has one); shorter ones go row by row.
+static constexpr int TC_MIN_Q = 16;
+
+extern "C" int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                   const int32_t* page_tables, int32_t num_seqs, int32_t total_q,
+                                   int32_t num_q_heads, int32_t max_pages_per_seq, int32_t max_kv_len,
+                                   const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                                   float scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                   pkv_stream_t stream) {
+  int st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || total_q < 0 || num_q_heads < 1 || max_kv_len < 0) return PKV_E_SHAPE;
+  if (num_q_heads % cache->num_kv_heads != 0) return PKV_E_SHAPE;
+  if (!head_dim_supported(cache->head_dim) || !group_supported(num_q_heads / cache->num_kv_heads))
+    return PKV_E_SHAPE;
+  if (total_q > 0 && max_pages_per_seq < 1) return PKV_E_SHAPE;
+  if ((int64_t)max_pages_per_seq * cache->page_size > INT32_MAX) return PKV_E_SHAPE;
+  if (total_q == 0) return PKV_OK;
+  if (!q || !cu_seqlens_q || !kv_lens || !page_tables || !k_cache || !v_cache || !out || !workspace)
+    return PKV_E_NULL;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) || ((uintptr_t)lse & 3u))
+    return PKV_E_ALIGN;
+  if (((uintptr_t)workspace & 255u) != 0) return PKV_E_WORKSPACE;
+  const PlanLayout lay =
+      plan_layout(num_seqs, total_q, num_q_heads, cache->num_kv_heads, cache->head_dim, max_kv_len);
+  if (workspace_bytes < lay.total) return PKV_E_WORKSPACE;
+  const DeviceFacts* f = device_facts();
+  if (!f) return PKV_E_CUDA;
+  if (!f->ok) return PKV_E_DEVICE;
+  cudaStream_t s = (cudaStream_t)stream;
+
+  const bool tc = prefill_tc_supported(cache->dtype, cache->head_dim, cache->page_size) && total_q >= TC_MIN_Q;
+
+  PlanArgs pa{};
+  pa.cu = cu_seqlens_q;
+  pa.kv_lens = kv_lens;
+  pa.B = num_seqs;
+  pa.T = total_q;
+  pa.Hq = num_q_heads;
+  pa.Hkv = cache->num_kv_heads;
+  pa.max_kv_len = max_kv_len;
+  pa.table_cap = max_pages_per_seq * cache->page_size;
+  // Split size depends only on the element size and head_dim (about 1 MB of K+V
+  // per item), never on the other rows of the tick, so a row's result does
+  // not change with the batch it is packed into. It only grows when the
+  // partial results would overflow the workspace.
+  {
+    const int elt = cache->dtype == PKV_F32 ? 4 : 2;
+    int c = (1 << 20) / (2 * cache->head_dim * elt);
+    pa.chunk_min = c < 256 ? 256 : c;
+  }
+  pa.target_items = 1 << 30;
+  pa.tc_min_q = tc ? TC_MIN_Q : 0;
+  pa.ws = (char*)workspace;
+  pa.lay = lay;
+  pa.dev_status = f->status;
+  cudaError_t e = launch_plan(pa, s);
+  if (e != cudaSuccess) return PKV_E_CUDA;
+
+  AttnArgs aa{};
+  aa.q = q;
+  aa.cu = cu_seqlens_q;
+  aa.kv_lens = kv_lens;
+  aa.page_tables = page_tables;
+  aa.B = num_seqs;
+  aa.T = total_q;
+  aa.Hq = num_q_heads;
+  aa.Hkv = cache->num_kv_heads;
+  aa.D = cache->head_dim;
+  aa.P = cache->page_size;
+  aa.num_pages = cache->num_pages;
+  aa.max_pages = max_pages_per_seq;
+  aa.k_cache = k_cache;
+  aa.v_cache = v_cache;
+  aa.scale = scale;
+  aa.out = out;
+  aa.lse = lse;
+  aa.ws = (char*)workspace;
+  aa.lay = lay;
+  aa.dtype = cache->dtype;
+  aa.num_sms = f->num_sms;
+  aa.dev_status = f->status;
+  if (tc) {
+    e = launch_prefill_tc(aa, s);
+    if (e != cudaSuccess) return PKV_E_CUDA;
+  }
+  e = launch_rows(aa, s);
+  if (e != cudaSuccess) return PKV_E_CUDA;
+  e = launch_combine(aa, s);
+  if (e != cudaSuccess) return PKV_E_CUDA;
+  return PKV_OK;
+}
+
+extern "C" int pkv_get_device_status(int32_t* code, pkv_stream_t stream) {
+  if (!code) return PKV_E_NULL;
+  const DeviceFacts* f = device_facts();
+  if (!f) return PKV_E_CUDA;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return PKV_E_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(v)) != cudaSuccess) return PKV_E_CUDA;
+  const int32_t zero = 0;
+  if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero)) != cudaSuccess) return PKV_E_CUDA;
+  *code = v;
+  return PKV_OK;
+}
+
+extern "C" int pkv_set_kernel_timing(int enable) {
+  std::lock_guard<std::mutex> lk(g_t_mu);
+  g_timing = enable != 0;
+  return PKV_OK;
+}
+
+extern "C" int pkv_kernel_times(const char** names, int32_t* launches, double* total_ms, int32_t max) {
+  std::lock_guard<std::mutex> lk(g_t_mu);
+  int n = 0;
+  int status = PKV_OK;
+  for (TimingRec& r : g_recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess)
+      status = PKV_E_CUDA;
+    int k = 0;
+    while (k < n && strcmp(names[k], r.name) != 0) ++k;
+    if (k == n) {
+      if (n >= max) continue;
+      names[n] = r.name;
+      launches[n] = 0;
+      total_ms[n] = 0.0;
+      ++n;
+    }
+    launches[k] += 1;
+    total_ms[k] += ms;
+  }
+  for (TimingRec& r : g_recs) {
+    g_free_events.push_back(r.a);
+    g_free_events.push_back(r.b);
+  }
+  g_recs.clear();
+  return status == PKV_OK ? n : status;
+}

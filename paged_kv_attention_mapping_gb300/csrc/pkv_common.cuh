@@ -1,0 +1,59 @@
+// Device helpers shared by the kernels of libpagedkv (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace pkv {
+
+// --- element conversion ------------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// Load N consecutive elements of T (N * sizeof(T) in {4, 8, 16} bytes) as floats.
+template <typename T, int N>
+__device__ __forceinline__ void load_as_f32(const T* p, float (&out)[N]) {
+  constexpr int BYTES = N * (int)sizeof(T);
+  static_assert(BYTES == 4 || BYTES == 8 || BYTES == 16 || BYTES == 32, "vector width");
+  if constexpr (BYTES == 32) {
+    load_as_f32<T, N / 2>(p, *reinterpret_cast<float(*)[N / 2]>(&out[0]));
+    load_as_f32<T, N / 2>(p + N / 2, *reinterpret_cast<float(*)[N / 2]>(&out[N / 2]));
+  } else {
+    using V = typename std::conditional<BYTES == 16, uint4, typename std::conditional<BYTES == 8, uint2, uint32_t>::type>::type;
+    V raw = __ldg(reinterpret_cast<const V*>(p));
+    const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+    for (int i = 0; i < N; ++i) out[i] = to_f32(e[i]);
+  }
+}
+
+// --- warp reductions ------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ void set_status(int32_t* ctrl_err, int32_t* dev_status, int bits) {
+  atomicOr(ctrl_err, bits);
+  atomicOr(dev_status, bits);
+}
+
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+}  // namespace pkv

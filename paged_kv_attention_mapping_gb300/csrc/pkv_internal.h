@@ -1,0 +1,105 @@
+// Internal declarations shared by the translation units of libpagedkv.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pagedkv.h"
+
+namespace pkv {
+
+// ---------------------------------------------------------------------------
+// device status word (one per device, in pkv_api.cu)
+int32_t* device_status_ptr();  // device address of the status word on the current device
+
+// ---------------------------------------------------------------------------
+// kernel timing hooks (pkv_api.cu). A KernelTimer brackets one launch with
+// CUDA events on its stream when timing is enabled.
+struct KernelTimer {
+  KernelTimer(const char* name, cudaStream_t s);
+  ~KernelTimer();
+  const char* name_;
+  cudaStream_t s_;
+  int slot_;
+};
+
+// ---------------------------------------------------------------------------
+// work plan held in the caller's workspace
+
+// Control words at the start of the workspace.
+enum Ctrl : int {
+  CTRL_ERR = 0,          // PKV_DEV_* bits seen by this call
+  CTRL_N_ITEMS = 1,      // row-path work items (row, kv head, split)
+  CTRL_ITEM_NEXT = 2,    // atomic work counter of the row kernel
+  CTRL_N_TILES = 3,      // tensor-core prefill tiles (seq, q tile, q head)
+  CTRL_TILE_NEXT = 4,    // atomic work counter of the prefill kernel
+  CTRL_CHUNK = 5,        // keys per split of a row-path (row, kv head)
+  CTRL_N_SPLIT_ROWS = 6, // rows whose keys were split
+  CTRL_N_PARTIALS = 7,   // partial results written
+  CTRL_N_PAIRS = 8,      // (seq, q tile) pairs of the prefill kernel
+  CTRL_WORDS = 64
+};
+
+struct PlanLayout {
+  size_t ctrl, row_seq, row_item_begin, row_part_begin, split_rows, seq_pair_begin, tc_pairs,
+      part_lse, part_o, total;
+  int32_t partial_cap;  // partial results the workspace can hold
+  int32_t pair_cap;     // (seq, q tile) pairs the workspace can hold
+};
+
+// Workspace layout for the given sizes (all offsets 256-byte aligned).
+PlanLayout plan_layout(int32_t num_seqs, int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t max_kv_len);
+
+// Rows of a tensor-core prefill tile and keys of a KV tile.
+constexpr int TC_BM = 128;
+constexpr int TC_BN = 128;
+
+struct PlanArgs {
+  const int32_t* cu;       // [B + 1]
+  const int32_t* kv_lens;  // [B]
+  int32_t B, T, Hq, Hkv;
+  int32_t max_kv_len, table_cap;  // table_cap = max_pages_per_seq * page_size
+  int32_t chunk_min;              // smallest split, keys (multiple of 64)
+  int32_t target_items;           // aim for about this many row-path items
+  int32_t tc_min_q;               // sequences with q_len >= this use the prefill kernel; 0 = never
+  char* ws;
+  PlanLayout lay;
+  int32_t* dev_status;
+};
+
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// kernels' host-side launchers
+
+struct AttnArgs {
+  const void* q;
+  const int32_t* cu;
+  const int32_t* kv_lens;
+  const int32_t* page_tables;
+  int32_t B, T, Hq, Hkv, D, P, num_pages, max_pages;
+  const void* k_cache;
+  const void* v_cache;
+  float scale;
+  void* out;
+  float* lse;
+  char* ws;
+  PlanLayout lay;
+  int dtype;
+  int num_sms;
+  int32_t* dev_status;
+};
+
+cudaError_t launch_append(const void* k, const void* v, const int64_t* slots, int32_t T, void* kc, void* vc,
+                          const pkv_cache_desc& c, cudaStream_t s);
+cudaError_t launch_rows(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_combine(const AttnArgs& a, cudaStream_t s);
+// Returns cudaErrorNotSupported when the shape has no tensor-core path.
+cudaError_t launch_prefill_tc(const AttnArgs& a, cudaStream_t s);
+bool prefill_tc_supported(int dtype, int D, int P);
+
+// workers of the row kernel (for the split policy)
+int rows_kernel_workers(int num_sms);
+
+}  // namespace pkv

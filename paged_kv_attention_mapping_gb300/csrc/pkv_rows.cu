@@ -1,0 +1,267 @@
+// Row path: attention of single query rows (decode tokens, and rows of short
+// chunks) over their sequence's pages, on CUDA cores, plus the split-KV merge.
+//
+// Helios blog, "torch.sdpa and Flash Attention": softmax(Q K^T / sqrt(d)) V,
+// with the query heads of one GQA group sharing one KV head. A work item is
+// (row, KV head, split): one warp streams that KV head's keys of the split
+// once, page by page through the page table, and serves all g query heads of
+// the group from each loaded key (online softmax in the exp2 domain with fp32
+// state, warp-shuffle reductions). Keys past the row's visible length are never
+// loaded, so stale or NaN slots cannot leak in. Items of rows whose keys were
+// split write a normalised partial (o, lse) into the workspace; the combine
+// kernel merges them: lse = ln sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s.
+#include <cuda_runtime.h>
+
+#include <type_traits>
+
+#include "pkv_common.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+constexpr int ROWS_WARPS = 4;
+constexpr int ROWS_BLOCKS_PER_SM = 8;
+
+int rows_kernel_workers(int num_sms) { return num_sms * ROWS_BLOCKS_PER_SM * ROWS_WARPS; }
+
+__device__ __forceinline__ int upper_bound_dev(const int32_t* a, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(a + mid) <= x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// U keys per step: loads of all U keys are issued before the math.
+template <typename T, int D, int G, int U>
+__global__ void __launch_bounds__(ROWS_WARPS * 32) rows_kernel(AttnArgs a) {
+  constexpr int DPL = D / 32;  // dims per lane
+  const int lane = threadIdx.x & 31;
+  int32_t* ctrl = (int32_t*)(a.ws + a.lay.ctrl);
+  const int32_t* item_begin = (const int32_t*)(a.ws + a.lay.row_item_begin);
+  const int32_t* part_begin = (const int32_t*)(a.ws + a.lay.row_part_begin);
+  float* part_o = (float*)(a.ws + a.lay.part_o);
+  float* part_lse = (float*)(a.ws + a.lay.part_lse);
+  const int n_items = *(volatile int32_t*)&ctrl[CTRL_N_ITEMS];
+  const int C = *(volatile int32_t*)&ctrl[CTRL_CHUNK];
+  const T* __restrict__ kc = (const T*)a.k_cache;
+  const T* __restrict__ vc = (const T*)a.v_cache;
+  const T* __restrict__ qp = (const T*)a.q;
+  const int64_t kstride = (int64_t)a.Hkv * D;  // elements between consecutive slots
+  const float qscale = a.scale * LOG2E;
+
+  for (;;) {
+    int item = 0;
+    if (lane == 0) item = atomicAdd(&ctrl[CTRL_ITEM_NEXT], 1);
+    item = __shfl_sync(0xffffffffu, item, 0);
+    if (item >= n_items) break;
+    const int r = upper_bound_dev(item_begin, a.T + 1, item) - 1;
+    const int local = item - __ldg(item_begin + r);
+    const int nsplit = (__ldg(item_begin + r + 1) - __ldg(item_begin + r)) / a.Hkv;
+    const int kvh = local / nsplit;
+    const int sp = local - kvh * nsplit;
+    const int b = upper_bound_dev(a.cu, a.B + 1, r) - 1;
+    const int c0 = __ldg(a.cu + b);
+    const int qlen = __ldg(a.cu + b + 1) - c0;
+    const int L = __ldg(a.kv_lens + b);
+    const int limit = L - qlen + (r - c0) + 1;
+    const int k0 = sp * C;
+    const int k1 = min(limit, k0 + C);
+
+    float qr[G][DPL];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      load_as_f32<T, DPL>(qp + ((int64_t)r * a.Hq + kvh * G + h) * D + lane * DPL, qr[h]);
+#pragma unroll
+      for (int c = 0; c < DPL; ++c) qr[h][c] *= qscale;
+    }
+    float m[G], l[G], o[G][DPL];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+#pragma unroll
+      for (int c = 0; c < DPL; ++c) o[h][c] = 0.f;
+    }
+
+    const int32_t* pt = a.page_tables + (int64_t)b * a.max_pages;
+    bool bad_page = false;
+    int j = k0;
+    while (j < k1) {
+      const int pidx = j / a.P;
+      const int off = j - pidx * a.P;
+      const int page = __ldg(pt + pidx);
+      if (page < 0 || page >= a.num_pages) {
+        bad_page = true;
+        break;
+      }
+      const int n = min(a.P - off, k1 - j);
+      const int64_t base = ((int64_t)page * a.P + off) * kstride + (int64_t)kvh * D + lane * DPL;
+      for (int t = 0; t < n; t += U) {
+        float kf[U][DPL], vf[U][DPL];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (t + u < n) {
+            load_as_f32<T, DPL>(kc + base + (int64_t)(t + u) * kstride, kf[u]);
+            load_as_f32<T, DPL>(vc + base + (int64_t)(t + u) * kstride, vf[u]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) kf[u][c] = vf[u][c] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float s[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            float acc = 0.f;
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) acc = fmaf(qr[h][c], kf[u][c], acc);
+            s[u] = warp_sum(acc);
+            if (t + u >= n) s[u] = -INFINITY;
+          }
+          float mx = m[h];
+#pragma unroll
+          for (int u = 0; u < U; ++u) mx = fmaxf(mx, s[u]);
+          const float alpha = exp2f(m[h] - mx);
+          m[h] = mx;
+          float lsum = l[h] * alpha;
+#pragma unroll
+          for (int c = 0; c < DPL; ++c) o[h][c] *= alpha;
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const float p = exp2f(s[u] - mx);
+            lsum += p;
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) o[h][c] = fmaf(p, vf[u][c], o[h][c]);
+          }
+          l[h] = lsum;
+        }
+      }
+      j += n;
+    }
+    if (bad_page) {
+      if (lane == 0) set_status(&ctrl[CTRL_ERR], a.dev_status, PKV_DEV_BAD_PAGE);
+      continue;
+    }
+
+    if (nsplit == 1) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float inv = 1.f / l[h];
+        T* dst = (T*)a.out + ((int64_t)r * a.Hq + kvh * G + h) * D + lane * DPL;
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) dst[c] = from_f32<T>(o[h][c] * inv);
+        if (a.lse != nullptr && lane == 0) a.lse[(int64_t)r * a.Hq + kvh * G + h] = (m[h] + __log2f(l[h])) * LN2;
+      }
+    } else {
+      const int p = __ldg(part_begin + r) + local;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float inv = 1.f / l[h];
+        float* dst = part_o + ((int64_t)p * G + h) * D + lane * DPL;
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) dst[c] = o[h][c] * inv;
+        if (lane == 0) part_lse[(int64_t)p * G + h] = (m[h] + __log2f(l[h])) * LN2;
+      }
+    }
+  }
+}
+
+// One warp per (split row, q head).
+template <typename T, int D>
+__global__ void __launch_bounds__(256) combine_kernel(AttnArgs a) {
+  constexpr int DPL = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int32_t* ctrl = (const int32_t*)(a.ws + a.lay.ctrl);
+  const int32_t* item_begin = (const int32_t*)(a.ws + a.lay.row_item_begin);
+  const int32_t* part_begin = (const int32_t*)(a.ws + a.lay.row_part_begin);
+  const int32_t* split_rows = (const int32_t*)(a.ws + a.lay.split_rows);
+  const float* part_o = (const float*)(a.ws + a.lay.part_o);
+  const float* part_lse = (const float*)(a.ws + a.lay.part_lse);
+  const int n_rows = ctrl[CTRL_N_SPLIT_ROWS];
+  const int G = a.Hq / a.Hkv;
+  const int64_t total = (int64_t)n_rows * a.Hq;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t w = blockIdx.x * (int64_t)(blockDim.x / 32) + (threadIdx.x >> 5); w < total; w += warps) {
+    const int r = split_rows[w / a.Hq];
+    const int h = (int)(w % a.Hq);
+    const int kvh = h / G, hh = h - kvh * G;
+    const int nsplit = (item_begin[r + 1] - item_begin[r]) / a.Hkv;
+    const int p0 = part_begin[r] + kvh * nsplit;
+    float mx = -INFINITY;
+    for (int s = lane; s < nsplit; s += 32) mx = fmaxf(mx, part_lse[(int64_t)(p0 + s) * G + hh]);
+    mx = warp_max(mx);
+    float sum = 0.f;
+    for (int s = lane; s < nsplit; s += 32) sum += __expf(part_lse[(int64_t)(p0 + s) * G + hh] - mx);
+    sum = warp_sum(sum);
+    const float lse = mx + __logf(sum);
+    float acc[DPL];
+#pragma unroll
+    for (int c = 0; c < DPL; ++c) acc[c] = 0.f;
+    for (int s = 0; s < nsplit; ++s) {
+      const float wgt = __expf(part_lse[(int64_t)(p0 + s) * G + hh] - lse);
+      const float* src = part_o + ((int64_t)(p0 + s) * G + hh) * D + lane * DPL;
+#pragma unroll
+      for (int c = 0; c < DPL; ++c) acc[c] = fmaf(wgt, src[c], acc[c]);
+    }
+    T* dst = (T*)a.out + ((int64_t)r * a.Hq + h) * D + lane * DPL;
+#pragma unroll
+    for (int c = 0; c < DPL; ++c) dst[c] = from_f32<T>(acc[c]);
+    if (a.lse != nullptr && lane == 0) a.lse[(int64_t)r * a.Hq + h] = lse;
+  }
+}
+
+template <typename T, int D, int G>
+static cudaError_t launch_rows_g(const AttnArgs& a, cudaStream_t s) {
+  constexpr int U = G >= 8 ? 2 : 4;
+  const int blocks = a.num_sms * ROWS_BLOCKS_PER_SM;
+  rows_kernel<T, D, G, U><<<blocks, ROWS_WARPS * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+static cudaError_t launch_rows_d(const AttnArgs& a, cudaStream_t s) {
+  switch (a.Hq / a.Hkv) {
+    case 1: return launch_rows_g<T, D, 1>(a, s);
+    case 2: return launch_rows_g<T, D, 2>(a, s);
+    case 4: return launch_rows_g<T, D, 4>(a, s);
+    case 8: return launch_rows_g<T, D, 8>(a, s);
+    case 16: return launch_rows_g<T, D, 16>(a, s);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+template <typename T>
+static cudaError_t launch_rows_t(const AttnArgs& a, cudaStream_t s) {
+  return a.D == 64 ? launch_rows_d<T, 64>(a, s) : launch_rows_d<T, 128>(a, s);
+}
+
+cudaError_t launch_rows(const AttnArgs& a, cudaStream_t s) {
+  KernelTimer timer("rows", s);
+  switch (a.dtype) {
+    case PKV_F32: return launch_rows_t<float>(a, s);
+    case PKV_F16: return launch_rows_t<__half>(a, s);
+    default: return launch_rows_t<__nv_bfloat16>(a, s);
+  }
+}
+
+template <typename T>
+static cudaError_t launch_combine_t(const AttnArgs& a, cudaStream_t s) {
+  const int blocks = a.num_sms * 2;
+  if (a.D == 64) combine_kernel<T, 64><<<blocks, 256, 0, s>>>(a);
+  else combine_kernel<T, 128><<<blocks, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const AttnArgs& a, cudaStream_t s) {
+  KernelTimer timer("combine", s);
+  switch (a.dtype) {
+    case PKV_F32: return launch_combine_t<float>(a, s);
+    case PKV_F16: return launch_combine_t<__half>(a, s);
+    default: return launch_combine_t<__nv_bfloat16>(a, s);
+  }
+}
+
+}  // namespace pkv

@@ -1,0 +1,116 @@
+"""The C-ABI library on the host: it loads, exports every call the header
+declares, and its host-only packing matches the oracle bit for bit (no GPU)."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_attention_mapping_gb300 import binding
+from paged_kv_attention_mapping_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_attention_mapping_gb300 import build
+    build.build()
+    return binding.lib()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_call(lib):
+    names = header_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(binding.EXPORTED)
+    assert "sm_103a" in binding.version()
+
+
+def test_status_strings(lib):
+    for code in range(-10, 1):
+        assert binding.status_string(code) not in ("", "unknown status")
+    assert binding.status_string(-99) == "unknown status"
+
+
+def _rand_requests(rng, B, P):
+    q_lens = [int(x) for x in rng.choice([0, 1, 1, 1, 2, 5, 17], size=B)]
+    kv = [max(q, 1) + int(rng.integers(0, 40)) for q in q_lens]
+    need = [-(-L // P) for L in kv]
+    extra = [int(rng.integers(0, 2)) for _ in range(B)]
+    n_pages = sum(n + e for n, e in zip(need, extra)) + 3
+    perm = [int(p) for p in rng.permutation(n_pages)]
+    pages, pos = [], 0
+    for n, e in zip(need, extra):
+        pages.append(perm[pos:pos + n + e])
+        pos += n + e
+    return q_lens, kv, pages, n_pages
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_pack_tick_matches_oracle(lib, seed):
+    rng = np.random.default_rng(seed)
+    P = int(rng.choice([1, 3, 16]))
+    q_lens, kv, pages, n_pages = _rand_requests(rng, int(rng.integers(1, 12)), P)
+    width = max(len(p) for p in pages) + int(rng.integers(0, 3))
+    got = binding.pack_tick(q_lens, kv, pages, P, n_pages, width)
+    want = oracle.pack_tick(q_lens, kv, pages, P, width)
+    for k in ("order", "cu_seqlens_q", "kv_lens", "page_tables", "slot_mapping"):
+        assert np.array_equal(got[k], want[k]), k
+
+
+@pytest.mark.parametrize("name", W.WORKLOADS)
+def test_pack_tick_matches_oracle_on_named_workloads(lib, name):
+    w = W.make_workload(name)
+    q = [r.q_len for r in w.requests]
+    kv = [r.kv_len for r in w.requests]
+    pg = [r.pages for r in w.requests]
+    got = binding.pack_tick(q, kv, pg, w.shape.page_size, w.num_pages)
+    want = oracle.pack_tick(q, kv, pg, w.shape.page_size)
+    for k in ("order", "cu_seqlens_q", "kv_lens", "page_tables", "slot_mapping"):
+        assert np.array_equal(got[k], want[k]), k
+
+
+def test_pack_tick_rejects_bad_inputs(lib):
+    ok = dict(q_lens=[1, 3], kv_lens=[4, 3], pages=[[0], [1]], page_size=4, num_pages=2)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return binding.pack_tick(a["q_lens"], a["kv_lens"], a["pages"], a["page_size"], a["num_pages"],
+                                 a.get("width"))
+
+    call()
+    with pytest.raises(binding.PagedKVError) as e:
+        call(kv_lens=[4, 2])                 # kv_len < q_len
+    assert e.value.status == -4
+    with pytest.raises(binding.PagedKVError) as e:
+        call(pages=[[0], [2]])               # page outside the pool
+    assert e.value.status == -5
+    with pytest.raises(binding.PagedKVError) as e:
+        call(kv_lens=[5, 3])                 # 5 tokens need 2 pages of 4
+    assert e.value.status == -5
+    with pytest.raises(binding.PagedKVError) as e:
+        call(q_lens=[-1, 3])
+    assert e.value.status == -4
+    with pytest.raises(binding.PagedKVError) as e:
+        call(page_size=0)
+    assert e.value.status == -3
+
+
+def test_workspace_size(lib):
+    import torch
+    kc = torch.empty((8, 16, 2, 64), dtype=torch.bfloat16)
+    n = binding.workspace_size(4, 10, 8, kc, 128)
+    assert n > 0 and n % 256 == 0
+    assert binding.workspace_size(4, 20, 8, kc, 128) >= n
+    with pytest.raises(binding.PagedKVError):
+        binding.workspace_size(4, 10, 7, kc, 128)   # Hq % Hkv != 0

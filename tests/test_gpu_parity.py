@@ -1,0 +1,273 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Append is compared bit for bit; attention within the tolerances of the
+workload description (max abs error 1e-2 bf16, 5e-3 fp16, 1e-4 fp32 on
+unit-normal inputs; lse 1e-3, 1e-5 for fp32). Every slot that no sequence owns
+below its kv_len is NaN-poisoned in the small cases, so a read of a slot the
+row may not see shows up as a NaN.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_attention_mapping_gb300 import binding
+from paged_kv_attention_mapping_gb300 import workloads as W
+
+from tick_helpers import (TOL_LSE, TOL_OUT, gpu_tick, idx_dev, lists, oracle_tick, poison_unused, sub_problem,
+                          to_dev, to_host)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from paged_kv_attention_mapping_gb300 import build
+    build.build()
+    binding.lib()
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    binding.device_status()  # clear
+    return d
+
+
+def run_and_compare(w, dev, poison=True, want_lse=True):
+    vals = W.host_values(w)
+    ql, kl, pg = lists(w)
+    packed = binding.pack_tick(ql, kl, pg, w.shape.page_size, w.num_pages)
+    kc_h, vc_h = vals.k_cache, vals.v_cache
+    if poison:
+        # NaN everywhere the tick will not own after the append
+        kc_h, vc_h = poison_unused(w, packed, kc_h, vc_h)
+    dt = w.shape.dtype
+    kc, vc = to_dev(kc_h, dt, dev), to_dev(vc_h, dt, dev)
+    out, lse = gpu_tick(w, packed, to_dev(vals.q, dt, dev), to_dev(vals.k_new, dt, dev), to_dev(vals.v_new, dt, dev),
+                        kc, vc, dev, want_lse=want_lse)
+    assert binding.device_status() == 0
+    ro, rl = oracle_tick(w, vals.q, vals.k_new, vals.v_new, kc_h, vc_h)
+    go = to_host(out).astype(np.float64)
+    assert np.isfinite(go).all()
+    eo = float(np.abs(go - ro).max())
+    assert eo <= TOL_OUT[dt], eo
+    if want_lse:
+        el = float(np.abs(lse.cpu().numpy() - rl).max())
+        assert el <= TOL_LSE[dt], el
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# append
+
+@pytest.mark.parametrize("name,dtype", [("tiny_decode", "f32"), ("tiny_decode", "bf16"),
+                                        ("tinyllama_decode", "f16")])
+def test_append_bit_exact(dev, name, dtype):
+    w = W.make_workload(name, dtype)
+    vals = W.host_values(w)
+    ql, kl, pg = lists(w)
+    packed = binding.pack_tick(ql, kl, pg, w.shape.page_size, w.num_pages)
+    kc, vc = to_dev(vals.k_cache, dtype, dev), to_dev(vals.v_cache, dtype, dev)
+    binding.kv_append(to_dev(vals.k_new, dtype, dev), to_dev(vals.v_new, dtype, dev),
+                      idx_dev(packed["slot_mapping"], dev), kc, vc)
+    torch.cuda.synchronize()
+    k2, v2 = oracle.kv_append(vals.k_cache, vals.v_cache, vals.k_new, vals.v_new, packed["slot_mapping"])
+    want_k = W.to_torch(k2, dtype)
+    want_v = W.to_torch(v2, dtype)
+    assert torch.equal(kc.cpu().view(torch.int16 if dtype != "f32" else torch.int32),
+                       want_k.view(torch.int16 if dtype != "f32" else torch.int32))
+    assert torch.equal(vc.cpu().view(torch.int16 if dtype != "f32" else torch.int32),
+                       want_v.view(torch.int16 if dtype != "f32" else torch.int32))
+
+
+def test_append_skips_negative_and_flags_out_of_pool_slots(dev):
+    N, P, H, D = 4, 16, 2, 64
+    kc = torch.zeros((N, P, H, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    k = torch.randn((3, H, D), device=dev).to(torch.bfloat16)
+    v = torch.randn((3, H, D), device=dev).to(torch.bfloat16)
+    binding.kv_append(k, v, torch.tensor([5, -1, N * P + 3], dtype=torch.int64, device=dev), kc, vc)
+    assert binding.device_status() == binding.DEV_BAD_SLOT
+    flat = kc.view(N * P, H, D)
+    assert torch.equal(flat[5], k[0])
+    assert int((flat != 0).any(dim=(1, 2)).sum()) == 1
+    assert binding.device_status() == 0
+
+
+# ---------------------------------------------------------------------------
+# attention, small cases against the whole oracle
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_tiny_decode(dev, dtype):
+    run_and_compare(W.make_workload("tiny_decode", dtype), dev)
+
+
+RAGGED = [
+    # seed, B, Hq, Hkv, d, P, dtype, q_lens, max_kv
+    (1, 8, 8, 2, 64, 16, "bf16", (1,), 300),
+    (2, 6, 32, 8, 128, 256, "bf16", (1, 2, 17), 300),
+    (3, 5, 32, 4, 64, 16, "f16", (1, 2, 17, 130), 300),
+    (4, 4, 8, 8, 128, 16, "f32", (1, 2, 17), 200),
+    (5, 3, 16, 2, 128, 256, "bf16", (130,), 300),
+    (6, 8, 4, 1, 64, 16, "f16", (1, 17), 300),
+    (7, 2, 32, 2, 64, 256, "bf16", (130, 1), 700),
+    (8, 7, 16, 16, 64, 16, "f32", (1,), 300),
+]
+
+
+@pytest.mark.parametrize("case", RAGGED, ids=[f"s{c[0]}-{c[6]}-d{c[4]}-P{c[5]}-g{c[2] // c[3]}" for c in RAGGED])
+def test_ragged(dev, case):
+    seed, B, Hq, Hkv, d, P, dt, ql, mk = case
+    w = W.random_workload(seed, B, Hq, Hkv, d, P, dt, ql, mk)
+    run_and_compare(w, dev)
+
+
+def test_without_lse(dev):
+    w = W.random_workload(11, 4, 8, 2, 64, 16, "bf16", (1, 17), 120)
+    run_and_compare(w, dev, want_lse=False)
+
+
+def test_idle_sequences_and_empty_tick(dev):
+    w = W.random_workload(12, 6, 8, 2, 64, 16, "bf16", (0, 1, 0, 5), 100)
+    run_and_compare(w, dev)
+    # a tick with no rows at all is a no-op that returns OK
+    kc = torch.zeros((2, 16, 2, 64), dtype=torch.bfloat16, device=dev)
+    q = torch.zeros((0, 8, 64), dtype=torch.bfloat16, device=dev)
+    ws = binding.alloc_workspace(1, 0, 8, kc, 16)
+    binding.paged_attention(q, torch.tensor([0, 0], dtype=torch.int32, device=dev),
+                            torch.tensor([5], dtype=torch.int32, device=dev),
+                            torch.zeros((1, 1), dtype=torch.int32, device=dev), kc, kc, 0.125, 16, workspace=ws)
+
+
+def test_packing_does_not_change_a_row(dev):
+    """A decode row gives bit-identical output alone and inside a mixed tick."""
+    w = W.random_workload(13, 6, 32, 8, 128, 256, "bf16", (1, 1, 40), 3000)
+    vals = W.host_values(w)
+    ql, kl, pg = lists(w)
+    packed = binding.pack_tick(ql, kl, pg, w.shape.page_size, w.num_pages)
+    dt = w.shape.dtype
+    kc, vc = to_dev(vals.k_cache, dt, dev), to_dev(vals.v_cache, dt, dev)
+    out, lse = gpu_tick(w, packed, to_dev(vals.q, dt, dev), to_dev(vals.k_new, dt, dev),
+                        to_dev(vals.v_new, dt, dev), kc, vc, dev)
+    cu = packed["cu_seqlens_q"]
+    order = packed["order"]
+    for b in range(len(order)):
+        if cu[b + 1] - cu[b] != 1:
+            continue
+        r = w.requests[order[b]]
+        one = W.Workload("one", w.shape, [r], w.num_pages, w.scale, w.seed)
+        p1 = binding.pack_tick([1], [r.kv_len], [r.pages], w.shape.page_size, w.num_pages)
+        q1 = to_dev(vals.q, dt, dev)[cu[b]:cu[b] + 1].contiguous()
+        o1, l1 = binding.paged_attention(q1, idx_dev(p1["cu_seqlens_q"], dev), idx_dev(p1["kv_lens"], dev),
+                                         idx_dev(p1["page_tables"], dev), kc, vc, w.scale, w.max_kv_len)
+        torch.cuda.synchronize()
+        assert torch.equal(o1[0], out[cu[b]]) and torch.equal(l1[0], lse[cu[b]])
+
+
+def test_bad_page_id_sets_status_and_skips_row(dev):
+    w = W.random_workload(14, 3, 8, 2, 64, 16, "bf16", (1,), 100)
+    vals = W.host_values(w)
+    ql, kl, pg = lists(w)
+    packed = binding.pack_tick(ql, kl, pg, w.shape.page_size, w.num_pages)
+    tables = packed["page_tables"].copy()
+    tables[1, 0] = w.num_pages + 7          # outside the pool
+    dt = w.shape.dtype
+    kc, vc = to_dev(vals.k_cache, dt, dev), to_dev(vals.v_cache, dt, dev)
+    out = torch.full((w.total_q, 8, 64), 7.0, dtype=torch.bfloat16, device=dev)
+    binding.paged_attention(to_dev(vals.q, dt, dev), idx_dev(packed["cu_seqlens_q"], dev),
+                            idx_dev(packed["kv_lens"], dev), idx_dev(tables, dev), kc, vc, w.scale, w.max_kv_len,
+                            out=out)
+    assert binding.device_status() & binding.DEV_BAD_PAGE
+    assert bool((out[1].float() == 7.0).all())           # the bad row is left unwritten
+    assert not bool((out[0].float() == 7.0).all())
+    assert binding.device_status() == 0
+
+
+def test_bad_lengths_set_status(dev):
+    kc = torch.zeros((4, 16, 2, 64), dtype=torch.bfloat16, device=dev)
+    q = torch.zeros((3, 8, 64), dtype=torch.bfloat16, device=dev)
+    binding.paged_attention(q, torch.tensor([0, 1, 3], dtype=torch.int32, device=dev),
+                            torch.tensor([40, 1], dtype=torch.int32, device=dev),   # 40 > 2 pages * 16; 1 < 2
+                            torch.zeros((2, 2), dtype=torch.int32, device=dev), kc, kc, 0.125, 64)
+    assert binding.device_status() & binding.DEV_BAD_LENGTHS
+
+
+def test_host_checks_reject_without_launch(dev):
+    kc = torch.zeros((4, 16, 2, 64), dtype=torch.bfloat16, device=dev)
+    q = torch.zeros((1, 6, 64), dtype=torch.bfloat16, device=dev)   # 6 % 4... Hq=6, Hkv=2 -> g=3 unsupported
+    with pytest.raises(binding.PagedKVError) as e:
+        binding.paged_attention(q, torch.tensor([0, 1], dtype=torch.int32, device=dev),
+                                torch.tensor([1], dtype=torch.int32, device=dev),
+                                torch.zeros((1, 1), dtype=torch.int32, device=dev), kc, kc, 0.1, 16,
+                                workspace=torch.empty(1 << 20, dtype=torch.uint8, device=dev))
+    assert e.value.status == -3
+    q = torch.zeros((1, 8, 64), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(binding.PagedKVError) as e:
+        binding.paged_attention(q, torch.tensor([0, 1], dtype=torch.int32, device=dev),
+                                torch.tensor([1], dtype=torch.int32, device=dev),
+                                torch.zeros((1, 1), dtype=torch.int32, device=dev), kc, kc, 0.1, 16,
+                                workspace=torch.empty(256, dtype=torch.uint8, device=dev))
+    assert e.value.status == -6
+
+
+# ---------------------------------------------------------------------------
+# the named workloads at full size, on sampled sequences and rows
+
+def full_size_check(name, dev, n_decode=12, chunk_rows=48, seed=0):
+    w = W.make_workload(name)
+    dt = w.shape.dtype
+    ql, kl, pg = lists(w)
+    packed = binding.pack_tick(ql, kl, pg, w.shape.page_size, w.num_pages)
+    ref = oracle.pack_tick(ql, kl, pg, w.shape.page_size)
+    for k in ref:
+        assert np.array_equal(packed[k], ref[k]), k
+    vals = W.device_values(w, dev)
+    # host copies of what the oracle needs, taken before the append
+    host_q, host_k, host_v = (to_host(vals[k]) for k in ("q", "k_new", "v_new"))
+    kc, vc = vals["k_cache"], vals["v_cache"]
+    cu = packed["cu_seqlens_q"]
+    B = len(packed["order"])
+    rng = np.random.default_rng(seed)
+    dec = [b for b in range(B) if cu[b + 1] - cu[b] == 1]
+    chunks = [b for b in range(B) if cu[b + 1] - cu[b] > 1]
+    seqs = sorted(set(rng.choice(dec, size=min(n_decode, len(dec)), replace=False).tolist()) | set(chunks))
+    # always include the longest decode sequence
+    if dec:
+        seqs = sorted(set(seqs) | {max(dec, key=lambda b: packed["kv_lens"][b])})
+    page_ids_cache = {}
+
+    def pages_of(cache):
+        def get(ids):
+            t = cache[torch.tensor(ids, device=dev, dtype=torch.long)]
+            return to_host(t)
+        return get
+
+    sub, rows, q_s, k_s, v_s, kc_s, vc_s = sub_problem(w, packed, seqs, host_q, host_k, host_v,
+                                                       pages_of(kc), pages_of(vc))
+    out, lse = gpu_tick(w, packed, vals["q"], vals["k_new"], vals["v_new"], kc, vc, dev)
+    assert binding.device_status() == 0
+    # rows to check: all decode rows of the sample, and a spread of chunk rows
+    sub_cu = oracle.pack_tick(*lists(sub), sub.shape.page_size)["cu_seqlens_q"]
+    check = []
+    for i in range(len(seqs)):
+        n = sub_cu[i + 1] - sub_cu[i]
+        if n <= 1:
+            check += list(range(sub_cu[i], sub_cu[i + 1]))
+        else:
+            pick = set(rng.choice(n, size=min(chunk_rows, n), replace=False).tolist()) | {0, n - 1, min(127, n - 1),
+                                                                                         min(128, n - 1)}
+            check += [sub_cu[i] + j for j in sorted(pick)]
+    ro, rl = oracle_tick(sub, q_s, k_s, v_s, kc_s, vc_s, rows=check)
+    go = to_host(out)[rows[check]].astype(np.float64)
+    gl = lse.cpu().numpy()[rows[check]]
+    eo = float(np.abs(go - ro).max())
+    el = float(np.abs(gl - rl).max())
+    assert np.isfinite(go).all()
+    assert eo <= TOL_OUT[dt], eo
+    assert el <= TOL_LSE[dt], el
+    return out, lse
+
+
+@pytest.mark.parametrize("name", ["tinyllama_decode", "qwen3_decode", "mixed_tick", "shared_prefix_long"])
+def test_full_size_workload(dev, name):
+    full_size_check(name, dev)
