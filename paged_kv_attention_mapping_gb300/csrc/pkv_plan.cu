@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a, int32_t* dev_sta
     if (tid == 0) s_cnt = 0;
     __syncthreads();
     if (total <= a.lay.partial_cap || C >= c_max) break;
-    C *= 2;
+    C = C * 2 < c_max ? C * 2 : c_max;
   }
 
   // pass 2: per-row item and partial ranges, and the list of split rows
