@@ -189,6 +189,39 @@ int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, const int32_
                         void* workspace, size_t workspace_bytes, pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * pkv_paged_attention_no_alloc — pkv_paged_attention without a workspace
+ * argument, for callers that cannot allocate device memory (for example code
+ * running inside a memory pool's or custom allocator's own callbacks, or a
+ * plug-in that is handed only the tensors it reads and writes). The serving
+ * pages have no counterpart of this call; it is a deployment convenience.
+ *
+ * Arguments, results, layouts and errors are those of pkv_paged_attention,
+ * minus workspace/workspace_bytes. The scratch the call needs (its work plan
+ * and split-KV partial results) lives in a fixed array of
+ * PKV_NO_ALLOC_SCRATCH_BYTES inside the library's device image, which every
+ * GPU that loads the library holds until the process exits. The call itself
+ * calls no cudaMalloc, cudaFree or allocating library routine.
+ *  - Limit: sizes whose work plan does not fit the array (very many packed
+ *    rows) return PKV_E_WORKSPACE; the split-KV partials get the room that is
+ *    left, and the split size grows until they fit.
+ *  - Set-up: the first call on each device looks up the array's device address
+ *    (with that device current); make that first call before any stream
+ *    capture.
+ *  - Sharing: every call on a device uses the same array, which keeps the last
+ *    call's contents; each call rewrites every counter and control word it
+ *    reads before using it. Calls that overlap on the GPU (for example on two
+ *    streams at once) race on the array and give undefined results: serialise
+ *    them.
+ */
+#define PKV_NO_ALLOC_SCRATCH_BYTES (16u << 20)
+
+int pkv_paged_attention_no_alloc(const void* q, const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                 const int32_t* page_tables, int32_t num_seqs, int32_t total_q,
+                                 int32_t num_q_heads, int32_t max_pages_per_seq, int32_t max_kv_len,
+                                 const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                                 float scale, void* out, float* lse, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Status and instrumentation. */
 
 /* Human-readable text for a pkv_status code (static storage). */

@@ -24,6 +24,7 @@ EXPORTED = (
     "pkv_kv_append",
     "pkv_paged_attention_workspace_size",
     "pkv_paged_attention",
+    "pkv_paged_attention_no_alloc",
     "pkv_status_string",
     "pkv_get_device_status",
     "pkv_set_kernel_timing",
@@ -66,6 +67,9 @@ def lib():
     L.pkv_paged_attention.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp,
                                       ctypes.POINTER(CacheDesc), ctypes.c_float, vp, vp, vp, sz, vp]
     L.pkv_paged_attention.restype = ctypes.c_int
+    L.pkv_paged_attention_no_alloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp,
+                                               ctypes.POINTER(CacheDesc), ctypes.c_float, vp, vp, vp]
+    L.pkv_paged_attention_no_alloc.restype = ctypes.c_int
     L.pkv_status_string.argtypes = [ctypes.c_int]
     L.pkv_status_string.restype = ctypes.c_char_p
     L.pkv_get_device_status.argtypes = [P32, vp]
@@ -216,6 +220,27 @@ def paged_attention(q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_cache, sca
                                    ctypes.byref(desc), ctypes.c_float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
                                    int(workspace.numel()), _stream_ptr(stream))
     _check(st, "pkv_paged_attention")
+    return out, lse
+
+
+def paged_attention_no_alloc(q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_cache, scale: float,
+                             max_kv_len: int, out=None, lse=None, want_lse: bool = True, stream=None):
+    """pkv_paged_attention_no_alloc: as paged_attention, but the library uses its
+    own fixed device scratch array instead of a caller workspace (for callers
+    that cannot allocate device memory). Output buffers may still be passed in."""
+    import torch
+    T, Hq, D = q.shape
+    B = int(cu_seqlens_q.shape[0]) - 1
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
+    desc = cache_desc(k_cache)
+    st = lib().pkv_paged_attention_no_alloc(_ptr(q), _ptr(cu_seqlens_q), _ptr(kv_lens), _ptr(page_tables), B,
+                                            int(T), int(Hq), int(page_tables.shape[1]), int(max_kv_len),
+                                            _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), ctypes.c_float(scale),
+                                            _ptr(out), _ptr(lse), _stream_ptr(stream))
+    _check(st, "pkv_paged_attention_no_alloc")
     return out, lse
 
 
