@@ -75,6 +75,8 @@ typedef enum {
                                    that sequence's rows are skipped */
 #define PKV_DEV_BAD_PAGE 0x4    /* attention: a page id needed by a row is outside the pool;
                                    that row's output is left unwritten */
+#define PKV_DEV_TIMEOUT 0x8     /* a kernel's internal wait gave up (a bug, never expected);
+                                   the outputs of that call are unspecified */
 
 /* One layer's K (or V) page pool: contiguous
  * [num_pages, page_size, num_kv_heads, head_dim] of `dtype`. */

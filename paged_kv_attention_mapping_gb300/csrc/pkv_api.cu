@@ -155,7 +155,7 @@ extern "C" size_t pkv_paged_attention_workspace_size(int32_t num_seqs, int32_t t
 
 // Sequences whose chunk has at least this many rows run on the tensor-core
 // prefill kernel (when the shape has one); shorter ones go row by row.
-static constexpr int TC_MIN_Q = 16;
+static constexpr int TC_MIN_Q = 64;
 
 extern "C" int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, const int32_t* kv_lens,
                                    const int32_t* page_tables, int32_t num_seqs, int32_t total_q,

@@ -58,7 +58,7 @@ const ScratchSetup* scratch_setup() {
   return &s;
 }
 
-constexpr int kTcMinQ = 16;  // same threshold as pkv_paged_attention
+constexpr int kTcMinQ = 64;  // same threshold as pkv_paged_attention
 
 }  // namespace
 }  // namespace pkv

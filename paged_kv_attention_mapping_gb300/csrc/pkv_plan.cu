@@ -52,6 +52,17 @@ __device__ __forceinline__ int upper_bound_i32(const int32_t* a, int n, int x) {
   return lo;
 }
 
+// Same search over an array this kernel wrote itself: plain loads, not the
+// read-only path, which is only coherent for data that is constant during the kernel.
+__device__ __forceinline__ int upper_bound_written(const volatile int32_t* a, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] <= x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
 // Exclusive scan over the 1024 threads of the block; *total gets the sum.
 __device__ int block_scan_excl(int v, int* total, int* sm) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -211,7 +222,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a, int32_t* dev_sta
   for (int i = tid; i < HIST; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   auto pair_work = [&](int p, int* b_out, int* qt_out) {
-    const int b = upper_bound_i32(pair_begin, a.B + 1, p) - 1;
+    const int b = upper_bound_written(pair_begin, a.B + 1, p) - 1;
     const int qt = p - pair_begin[b];
     const SeqInfo s = seq_info(a, b);
     const int q1 = min(s.q, (qt + 1) * TC_BM);
