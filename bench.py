@@ -390,7 +390,7 @@ def main():
             roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": ach / peaks["hbm_gbs"], "traffic": None, "algorithmic_per_launch": nbytes}
         roof["peak_source"] = peaks["source"]
-    decode_k = "rows" if "rows" in ktimes else None
+    decode_k = "decode" if "decode" in ktimes else ("rows" if "rows" in ktimes else None)
     decode_gbs = None
     if decode_k and work["decode_bytes"]:
         decode_gbs = work["decode_bytes"] / (ktimes[decode_k][1] / ktimes[decode_k][0] / 1000.0) / 1e9

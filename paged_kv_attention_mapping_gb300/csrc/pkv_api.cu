@@ -240,7 +240,7 @@ extern "C" int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, c
     e = launch_prefill_tc(aa, s);
     if (e != cudaSuccess) return PKV_E_CUDA;
   }
-  e = launch_rows(aa, s);
+  e = decode_supported(aa.dtype, aa.D, aa.P) ? launch_decode(aa, s) : launch_rows(aa, s);
   if (e != cudaSuccess) return PKV_E_CUDA;
   e = launch_combine(aa, s);
   if (e != cudaSuccess) return PKV_E_CUDA;

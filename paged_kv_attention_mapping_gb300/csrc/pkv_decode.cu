@@ -1,0 +1,743 @@
+// Decode attention: single query rows over their pages, HBM-bound.
+//
+// Helios blog, "torch.sdpa and Flash Attention": softmax(Q K^T / sqrt(d)) V,
+// with the query heads of a GQA group sharing one KV head, so one pass over a
+// KV head's keys serves the whole group; Helios README, "Paged attention": K/V
+// are read through the page table, never gathered into a dense copy.
+//
+// Work item = (row, KV head, split of the keys), from the device plan. One
+// CTA = 1 producer warp + 4 compute warps, two CTAs per SM, persistent:
+//  * producer: takes items from the plan (atomic counter) into a 2-deep item
+//    queue and streams each item's 64-key K and V tiles out of the page pool
+//    with TMA (128-byte swizzled boxes, one per page or 64-key run) into a
+//    3-stage shared-memory ring; it runs ahead across item boundaries.
+//  * compute warps: warp w owns keys 16w..16w+15 of every tile. QK: two lanes
+//    per key (each half of head_dim), q of all g heads broadcast from shared
+//    memory, packed fp32x2 FMAs, one shuffle to join the halves. Online softmax
+//    per warp (exp2 domain, shuffle reductions over the warp's keys). PV: lanes
+//    own head_dim/32 dims for all g heads, p broadcast by shuffle.
+//  * end of item: the 4 warps' (m, l, o) merge in shared memory; the result
+//    goes to out/lse, or to the workspace as a partial when the row was split.
+// Keys past the item's end are masked in QK and skipped in PV, so stale or NaN
+// slots never enter a sum. Every mbarrier wait is bounded (PKV_DEV_TIMEOUT).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "pkv_common.cuh"
+#include "pkv_internal.h"
+#include "pkv_sm100.cuh"
+
+namespace pkv {
+using namespace sm100;
+
+namespace {
+
+constexpr int BT = 64;             // keys per tile
+constexpr int NCW = 4;             // compute warps
+constexpr int NTHREADS = (NCW + 1) * 32;
+constexpr int CTAS_PER_SM = 2;
+
+struct DecParams {
+  const int32_t* cu;
+  const int32_t* kv_lens;
+  const int32_t* page_tables;
+  const void* q;
+  int B, T, Hq, Hkv, P, num_pages, max_pages;
+  float scale_log2;
+  void* out;
+  float* lse;
+  int32_t* ctrl;
+  const int32_t* item_begin;
+  const int32_t* part_begin;
+  float* part_o;
+  float* part_lse;
+  int32_t* dev_status;
+};
+
+struct Item {
+  int valid;
+  int r, kvh, b, k0, k1, nsplit, local;
+  int n_tiles;
+};
+
+template <typename T>
+struct Elt {
+  static constexpr int BYTES = sizeof(T);
+};
+
+// 8 bytes of T -> floats (4 bf16/f16 or 2 f32)
+__device__ __forceinline__ void cvt16(const uint4& raw, float2 (&o)[4], __nv_bfloat16*) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+}
+__device__ __forceinline__ void cvt16(const uint4& raw, float2 (&o)[4], __half*) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[i] = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+}
+__device__ __forceinline__ void cvt16(const uint4& raw, float2 (&o)[2], float*) {
+  o[0] = make_float2(__uint_as_float(raw.x), __uint_as_float(raw.y));
+  o[1] = make_float2(__uint_as_float(raw.z), __uint_as_float(raw.w));
+}
+
+template <typename T>
+__device__ __forceinline__ float2 cvt_pair(uint32_t w);
+template <>
+__device__ __forceinline__ float2 cvt_pair<__nv_bfloat16>(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+template <>
+__device__ __forceinline__ float2 cvt_pair<__half>(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
+__device__ __forceinline__ bool wait_flag(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* ctrl,
+                                          int32_t* dev_status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > 2000000000ull || it > (1u << 28)) {
+        *abort_flag = 1;
+        atomicOr(&ctrl[CTRL_ERR], PKV_DEV_TIMEOUT);
+        atomicOr(dev_status, PKV_DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ int upper_bound_c(const int32_t* a, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(a + mid) <= x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// --- mma.sync m16n8k16 helpers (16-bit A/B, fp32 accumulators) -------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+template <typename T>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+template <typename T>
+__device__ __forceinline__ uint32_t pack2h(float a, float b) {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+template <typename T, int D, int G>
+struct DCfg {
+  static constexpr int ELT = sizeof(T);
+  static constexpr int ROW_BYTES = D * ELT;            // one key of one KV head
+  static constexpr int ATOMS = ROW_BYTES / 128;        // 128-byte swizzle atoms per key row
+  static constexpr int ATOM_ELEMS = 128 / ELT;
+  static constexpr int TILE_BYTES = BT * ROW_BYTES;    // K (or V) tile
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int NST = STAGE_BYTES <= 32768 ? 3 : 2;
+  static constexpr int Q_BYTES = G * D * 4;
+  static constexpr int MERGE_BYTES = NCW * G * D * 4 + NCW * G * 8;
+  static constexpr int SMEM = NST * STAGE_BYTES + Q_BYTES + MERGE_BYTES + 1024;
+  static constexpr int DPL = D / 32;                   // PV: dims per lane
+  static_assert(ROW_BYTES % 128 == 0, "key rows must be whole swizzle atoms");
+};
+
+// address of 16-byte chunk `chunk16` (byte offset chunk16*16 in the key row) of tile row `row`
+template <int ATOMS>
+__device__ __forceinline__ uint32_t sw_addr(uint32_t tile_base, int row, int byte_off) {
+  const int atom = byte_off >> 7;
+  const int ch = (byte_off >> 4) & 7;
+  return tile_base + atom * (BT * 128) + row * 128 + ((ch ^ (row & 7)) << 4) + (byte_off & 15);
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
+    decode_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv, DecParams p) {
+  using C = DCfg<T, D, G>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  unsigned char* sStage = sm;
+  float* sQ = (float*)(sm + C::NST * C::STAGE_BYTES);
+  float* sMergeO = sQ + G * D;                   // [NCW][G][D]
+  float* sMergeML = sMergeO + NCW * G * D;       // [NCW][G][2]
+
+  __shared__ __align__(8) uint64_t bar_full[C::NST], bar_empty[C::NST], bar_ifull[2], bar_iempty[2], bar_cw;
+  __shared__ Item s_item[2];
+  __shared__ int s_bad[2];
+  __shared__ volatile int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], NCW);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_ifull[s], 1);
+      mbar_init(&bar_iempty[s], NCW);
+    }
+    mbar_init(&bar_cw, NCW * 32);
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  __syncthreads();
+  const int n_items = *(volatile int32_t*)&p.ctrl[CTRL_N_ITEMS];
+  const int Cchunk = *(volatile int32_t*)&p.ctrl[CTRL_CHUNK];
+
+  if (warp == NCW) {
+    // ================================================================ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mk);
+      tma_prefetch_desc(&mv);
+    }
+    uint32_t stage_use = 0;
+    for (uint32_t it = 0;; ++it) {
+      const int slot = it & 1;
+      if (!__all_sync(0xffffffffu, wait_flag(&bar_iempty[slot], ((it >> 1) & 1) ^ 1, &s_abort, p.ctrl,
+                                             p.dev_status)))
+        break;
+      Item item;
+      item.valid = 0;
+      if (lane == 0) {
+        const int i = s_abort ? n_items : atomicAdd(&p.ctrl[CTRL_ITEM_NEXT], 1);
+        if (i < n_items) {
+          const int r = upper_bound_c(p.item_begin, p.T + 1, i) - 1;
+          const int b0 = __ldg(p.item_begin + r);
+          item.local = i - b0;
+          item.nsplit = (__ldg(p.item_begin + r + 1) - b0) / p.Hkv;
+          item.kvh = item.local / item.nsplit;
+          const int sp = item.local - item.kvh * item.nsplit;
+          const int b = upper_bound_c(p.cu, p.B + 1, r) - 1;
+          const int c0 = __ldg(p.cu + b);
+          const int qlen = __ldg(p.cu + b + 1) - c0;
+          const int L = __ldg(p.kv_lens + b);
+          const int limit = L - qlen + (r - c0) + 1;
+          item.r = r;
+          item.b = b;
+          item.k0 = sp * Cchunk;
+          item.k1 = min(limit, item.k0 + Cchunk);
+          item.n_tiles = (item.k1 - item.k0 + BT - 1) / BT;
+          item.valid = 1;
+        }
+        s_item[slot] = item;
+        s_bad[slot] = 0;
+        mbar_arrive(&bar_ifull[slot]);
+      }
+      item.valid = __shfl_sync(0xffffffffu, item.valid, 0);
+      if (!item.valid) break;
+      item.b = __shfl_sync(0xffffffffu, item.b, 0);
+      item.kvh = __shfl_sync(0xffffffffu, item.kvh, 0);
+      item.k0 = __shfl_sync(0xffffffffu, item.k0, 0);
+      item.k1 = __shfl_sync(0xffffffffu, item.k1, 0);
+      item.n_tiles = __shfl_sync(0xffffffffu, item.n_tiles, 0);
+      const int32_t* pt = p.page_tables + (int64_t)item.b * p.max_pages;
+      bool ok = true;
+      for (int t = 0; t < item.n_tiles; ++t) {
+        const uint32_t st = stage_use % C::NST, round = stage_use / C::NST;
+        ++stage_use;
+        if (!__all_sync(0xffffffffu, wait_flag(&bar_empty[st], (round & 1) ^ 1, &s_abort, p.ctrl, p.dev_status))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          unsigned char* kdst = sStage + st * C::STAGE_BYTES;
+          unsigned char* vdst = kdst + C::TILE_BYTES;
+          const int kb = item.k0 + t * BT;
+          if (p.P >= BT) {
+            const int lp = kb / p.P;
+            const int page = __ldg(pt + lp);
+            if (page < 0 || page >= p.num_pages) {
+              s_bad[slot] = 1;
+              mbar_arrive(&bar_full[st]);
+            } else {
+              const int row = page * p.P + (kb - lp * p.P);
+              mbar_arrive_expect_tx(&bar_full[st], 2 * C::TILE_BYTES);
+#pragma unroll
+              for (int a = 0; a < C::ATOMS; ++a) {
+                tma_load_3d(kdst + a * BT * 128, &mk, &bar_full[st], a * C::ATOM_ELEMS, item.kvh, row);
+                tma_load_3d(vdst + a * BT * 128, &mv, &bar_full[st], a * C::ATOM_ELEMS, item.kvh, row);
+              }
+            }
+          } else {
+            const int per = BT / p.P;
+            const int lp0 = kb / p.P;
+            const int cnt = min(per, (item.k1 - kb + p.P - 1) / p.P);
+            bool bad = false;
+            for (int pp = 0; pp < cnt; ++pp) {
+              const int page = __ldg(pt + lp0 + pp);
+              bad |= page < 0 || page >= p.num_pages;
+            }
+            if (bad) {
+              s_bad[slot] = 1;
+              mbar_arrive(&bar_full[st]);
+            } else {
+              mbar_arrive_expect_tx(&bar_full[st], (uint32_t)(2 * cnt * p.P * C::ROW_BYTES));
+              for (int pp = 0; pp < cnt; ++pp) {
+                const int row = __ldg(pt + lp0 + pp) * p.P;
+#pragma unroll
+                for (int a = 0; a < C::ATOMS; ++a) {
+                  tma_load_3d(kdst + a * BT * 128 + pp * p.P * 128, &mk, &bar_full[st], a * C::ATOM_ELEMS, item.kvh,
+                              row);
+                  tma_load_3d(vdst + a * BT * 128 + pp * p.P * 128, &mv, &bar_full[st], a * C::ATOM_ELEMS, item.kvh,
+                              row);
+                }
+              }
+            }
+          }
+        }
+      }
+      if (!ok) break;
+    }
+    // let any copy this warp issued land before the CTA may exit
+    if (lane == 0) {
+      for (int s = 0; s < C::NST; ++s) {
+        const uint32_t uses = stage_use / C::NST + (s < (int)(stage_use % C::NST) ? 1 : 0);
+        if (uses > 0) mbar_wait(&bar_full[s], (uses - 1) & 1, 500000000ull);
+      }
+    }
+    return;
+  }
+
+  // ================================================================= compute
+  uint32_t stage_use = 0;
+  uint32_t cw_phase = 0;
+  // barrier of the 128 compute threads, bounded like every other wait
+  auto cw_sync = [&]() -> bool {
+    mbar_arrive(&bar_cw);
+    const bool ok = wait_flag(&bar_cw, cw_phase & 1, &s_abort, p.ctrl, p.dev_status);
+    ++cw_phase;
+    return __all_sync(0xffffffffu, ok);
+  };
+  const uint32_t stage0 = smem_u32(sStage);
+  constexpr bool MMA = C::ELT == 2;
+  const int grp = lane >> 2, tig = lane & 3;   // mma fragment coordinates
+  for (uint32_t it = 0;; ++it) {
+    const int slot = it & 1;
+    if (!__all_sync(0xffffffffu, wait_flag(&bar_ifull[slot], (it >> 1) & 1, &s_abort, p.ctrl, p.dev_status))) break;
+    const Item item = s_item[slot];
+    if (!item.valid) break;
+    const T* qg = (const T*)p.q + ((int64_t)item.r * p.Hq + item.kvh * G) * D;
+    if constexpr (!MMA) {
+      // q of the group, scaled into the exp2 domain, into shared memory
+      for (int e = tid; e < G * D; e += NCW * 32) sQ[e] = to_f32(qg[e]) * p.scale_log2;
+    }
+    // also keeps the previous item's merge reads ahead of this item's merge writes
+    if (!cw_sync()) break;
+    bool ok = true;
+    bool bad = false;
+    if constexpr (MMA) {
+      // ------------------------------------------------ tensor-core (mma.sync) path
+      // Q (the group's G heads as the 16 rows of the A operand, rows >= G zero)
+      uint32_t qa[D / 16][4];
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int c0 = kk * 16 + tig * 2;
+        auto ld2 = [&](int row, int col) -> uint32_t {
+          return row < G ? *reinterpret_cast<const uint32_t*>(qg + row * D + col) : 0u;
+        };
+        qa[kk][0] = ld2(grp, c0);
+        qa[kk][1] = ld2(grp + 8, c0);
+        qa[kk][2] = ld2(grp, c0 + 8);
+        qa[kk][3] = ld2(grp + 8, c0 + 8);
+      }
+      constexpr bool HI = G > 8;                 // rows grp + 8 are real heads
+      float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
+      float o[D / 8][4];
+#pragma unroll
+      for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+      for (int t = 0; t < item.n_tiles; ++t) {
+        const uint32_t st = stage_use % C::NST, round = stage_use / C::NST;
+        ++stage_use;
+        if (!__all_sync(0xffffffffu, wait_flag(&bar_full[st], round & 1, &s_abort, p.ctrl, p.dev_status))) {
+          ok = false;
+          break;
+        }
+        const uint32_t kbase = stage0 + st * C::STAGE_BYTES;
+        const uint32_t vbase = kbase + C::TILE_BYTES;
+        const int tile_keys = min(BT, item.k1 - (item.k0 + t * BT));
+        const int nvalid = min(16, tile_keys - warp * 16);   // this warp's keys in the tile (may be <= 0)
+        if (nvalid > 0) {
+          // keys past the end: zero their V rows so 0 * (stale or NaN) cannot reach O
+          if (nvalid < 16) {
+            for (int e = lane; e < (16 - nvalid) * (C::ROW_BYTES / 16); e += 32) {
+              const int rr = warp * 16 + nvalid + e / (C::ROW_BYTES / 16);
+              const int bo = (e % (C::ROW_BYTES / 16)) * 16;
+              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sw_addr<C::ATOMS>(vbase, rr, bo)),
+                           "r"(0u)
+                           : "memory");
+            }
+            __syncwarp();
+          }
+          // S = Q K^T for the warp's 16 keys (two n-tiles of 8)
+          float s[2][4];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk += 2) {
+              const int mtx = lane >> 3;
+              const int krow = warp * 16 + nt * 8 + (lane & 7);
+              const int dim = (kk + (mtx >> 1)) * 16 + (mtx & 1) * 8;
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(sw_addr<C::ATOMS>(kbase, krow, dim * 2), b0, b1, b2, b3);
+              mma16816<T>(s[nt], qa[kk], b0, b1);
+              mma16816<T>(s[nt], qa[kk + 1], b2, b3);
+            }
+          }
+          // online softmax over the warp's keys (rows: head grp, and grp + 8)
+          float pv[2][4];
+#pragma unroll
+          for (int hr = 0; hr < (HI ? 2 : 1); ++hr) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int key = nt * 8 + tig * 2 + e;
+                float v = s[nt][hr * 2 + e] * p.scale_log2;
+                v = key < nvalid ? v : -INFINITY;
+                s[nt][hr * 2 + e] = v;
+                mx = fmaxf(mx, v);
+              }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_new = fmaxf(m_run[hr], mx);
+            const float alpha = exp2f(m_run[hr] - m_new);
+            m_run[hr] = m_new;
+            float ls = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float pe = exp2f(s[nt][hr * 2 + e] - m_new);
+                pv[nt][hr * 2 + e] = pe;
+                ls += pe;
+              }
+            l_part[hr] = l_part[hr] * alpha + ls;
+#pragma unroll
+            for (int nd = 0; nd < D / 8; ++nd) {
+              o[nd][hr * 2] *= alpha;
+              o[nd][hr * 2 + 1] *= alpha;
+            }
+          }
+          if (!HI) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) pv[nt][2] = pv[nt][3] = 0.f;
+          }
+          // P as the A operand: keys 0-7 from n-tile 0, keys 8-15 from n-tile 1
+          uint32_t pa[4];
+          pa[0] = pack2h<T>(pv[0][0], pv[0][1]);
+          pa[1] = pack2h<T>(pv[0][2], pv[0][3]);
+          pa[2] = pack2h<T>(pv[1][0], pv[1][1]);
+          pa[3] = pack2h<T>(pv[1][2], pv[1][3]);
+          // O += P V over the warp's 16 keys
+#pragma unroll
+          for (int nd = 0; nd < D / 8; nd += 2) {
+            const int mtx = lane >> 3;
+            const int vrow = warp * 16 + (mtx & 1) * 8 + (lane & 7);
+            const int dim = (nd + (mtx >> 1)) * 8;
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(sw_addr<C::ATOMS>(vbase, vrow, dim * 2), b0, b1, b2, b3);
+            mma16816<T>(o[nd], pa, b0, b1);
+            mma16816<T>(o[nd + 1], pa, b2, b3);
+          }
+          if (nvalid < 16) fence_proxy_async_smem();   // our zeroing before the next TMA write
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_empty[st]);
+      }
+      bad = s_bad[slot] != 0;                          // final once the item's last tile landed
+      if (lane == 0) mbar_arrive(&bar_iempty[slot]);   // the item slot may be refilled
+      if (!__all_sync(0xffffffffu, ok)) break;
+      // this warp's state into shared memory
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int h = grp + hr * 8;
+        float l = l_part[hr];
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        if (h < G) {
+          if (tig == 0) {
+            sMergeML[(warp * G + h) * 2 + 0] = m_run[hr];
+            sMergeML[(warp * G + h) * 2 + 1] = l;
+          }
+#pragma unroll
+          for (int nd = 0; nd < D / 8; ++nd) {
+            float* dst = sMergeO + (warp * G + h) * D + nd * 8 + tig * 2;
+            dst[0] = o[nd][hr * 2];
+            dst[1] = o[nd][hr * 2 + 1];
+          }
+        }
+      }
+    } else {
+      // ------------------------------------------------ CUDA-core (fp32) path
+      const int j16 = lane & 15;        // QK: key within the warp's 16
+      const int half = lane >> 4;       // QK: which half of head_dim
+      float m_run[G], l_part[G];
+      float2 acc[G][C::DPL / 2 > 0 ? C::DPL / 2 : 1];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        m_run[h] = -INFINITY;
+        l_part[h] = 0.f;
+#pragma unroll
+        for (int c = 0; c < (C::DPL / 2 > 0 ? C::DPL / 2 : 1); ++c) acc[h][c] = make_float2(0.f, 0.f);
+      }
+      for (int t = 0; t < item.n_tiles; ++t) {
+        const uint32_t st = stage_use % C::NST, round = stage_use / C::NST;
+        ++stage_use;
+        if (!__all_sync(0xffffffffu, wait_flag(&bar_full[st], round & 1, &s_abort, p.ctrl, p.dev_status))) {
+          ok = false;
+          break;
+        }
+        const uint32_t kbase = stage0 + st * C::STAGE_BYTES;
+        const uint32_t vbase = kbase + C::TILE_BYTES;
+        const int tile_keys = min(BT, item.k1 - (item.k0 + t * BT));
+        const int row = warp * 16 + j16;
+        const int nvalid = min(16, tile_keys - warp * 16);   // keys of this warp in the tile (may be <= 0)
+        // ---- QK: lanes (j16, half) -> partial dot over half of head_dim
+        float s[G];
+        {
+          float2 a2[G];
+#pragma unroll
+          for (int h = 0; h < G; ++h) a2[h] = make_float2(0.f, 0.f);
+          constexpr int HB = C::ROW_BYTES / 2;           // bytes of half a key row
+#pragma unroll
+          for (int cb = 0; cb < HB; cb += 16) {
+            const int boff = half * HB + cb;
+            uint4 raw;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
+                         : "r"(sw_addr<C::ATOMS>(kbase, row, boff)));
+            constexpr int NE = 16 / C::ELT;              // elements in the chunk
+            float2 kf[NE / 2];
+            cvt16(raw, kf, (T*)nullptr);
+            const int d0 = boff / C::ELT;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              const float4* qv = reinterpret_cast<const float4*>(sQ + h * D + d0);
+#pragma unroll
+              for (int e = 0; e < NE / 4; ++e) {
+                const float4 q4 = qv[e];
+                a2[h] = __ffma2_rn(make_float2(q4.x, q4.y), kf[2 * e], a2[h]);
+                a2[h] = __ffma2_rn(make_float2(q4.z, q4.w), kf[2 * e + 1], a2[h]);
+              }
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            float v = a2[h].x + a2[h].y;
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            s[h] = j16 < nvalid ? v : -INFINITY;
+          }
+        }
+        // ---- online softmax over the warp's keys
+        float pr[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float mx = s[h];
+#pragma unroll
+          for (int o2 = 1; o2 < 16; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+          const float m_new = fmaxf(m_run[h], mx);
+          const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run[h] - m_new);
+          m_run[h] = m_new;
+          pr[h] = m_new == -INFINITY ? 0.f : exp2f(s[h] - m_new);
+          l_part[h] = l_part[h] * alpha + (half == 0 ? pr[h] : 0.f);
+#pragma unroll
+          for (int c = 0; c < (C::DPL / 2 > 0 ? C::DPL / 2 : 1); ++c)
+            acc[h][c] = __fmul2_rn(acc[h][c], make_float2(alpha, alpha));
+        }
+        // ---- PV: lanes own DPL dims of every head
+        for (int k = 0; k < nvalid; ++k) {
+          const int vrow = warp * 16 + k;
+          float pk[G];
+#pragma unroll
+          for (int h = 0; h < G; ++h) pk[h] = __shfl_sync(0xffffffffu, pr[h], k);
+          if constexpr (C::DPL * C::ELT == 8) {  // 2 x f32 per lane
+            uint2 raw;
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                         : "=r"(raw.x), "=r"(raw.y)
+                         : "r"(sw_addr<C::ATOMS>(vbase, vrow, lane * 8)));
+            const float2 v0 = make_float2(__uint_as_float(raw.x), __uint_as_float(raw.y));
+#pragma unroll
+            for (int h = 0; h < G; ++h) acc[h][0] = __ffma2_rn(make_float2(pk[h], pk[h]), v0, acc[h][0]);
+          } else {  // 4 x f32 per lane
+            uint4 raw;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
+                         : "r"(sw_addr<C::ATOMS>(vbase, vrow, lane * 16)));
+            const float2 v0 = make_float2(__uint_as_float(raw.x), __uint_as_float(raw.y));
+            const float2 v1 = make_float2(__uint_as_float(raw.z), __uint_as_float(raw.w));
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              acc[h][0] = __ffma2_rn(make_float2(pk[h], pk[h]), v0, acc[h][0]);
+              acc[h][1] = __ffma2_rn(make_float2(pk[h], pk[h]), v1, acc[h][1]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_empty[st]);
+      }
+      bad = s_bad[slot] != 0;
+      if (lane == 0) mbar_arrive(&bar_iempty[slot]);
+      if (!__all_sync(0xffffffffu, ok)) break;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float l = l_part[h];
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o2);
+        if (lane == 0) {
+          sMergeML[(warp * G + h) * 2 + 0] = m_run[h];
+          sMergeML[(warp * G + h) * 2 + 1] = l;
+        }
+        float* dst = sMergeO + (warp * G + h) * D + lane * C::DPL;
+#pragma unroll
+        for (int c = 0; c < C::DPL; ++c) dst[c] = (c & 1) ? acc[h][c >> 1].y : acc[h][c >> 1].x;
+      }
+    }
+    // ---- merge the 4 warps' states
+    if (!cw_sync()) break;
+    if (!bad) {
+      for (int e = tid; e < G * D; e += NCW * 32) {
+        const int h = e / D;
+        float m = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) m = fmaxf(m, sMergeML[(w * G + h) * 2]);
+        float l = 0.f, ov = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+          const float mw = sMergeML[(w * G + h) * 2];
+          const float sc = mw == -INFINITY ? 0.f : exp2f(mw - m);
+          l += sMergeML[(w * G + h) * 2 + 1] * sc;
+          ov += sMergeO[(w * G + h) * D + (e - h * D)] * sc;
+        }
+        ov /= l;
+        const float lse_n = (m + __log2f(l)) * LN2;
+        if (item.nsplit == 1) {
+          ((T*)p.out)[((int64_t)item.r * p.Hq + item.kvh * G) * D + e] = from_f32<T>(ov);
+          if (p.lse && (e - h * D) == 0) p.lse[(int64_t)item.r * p.Hq + item.kvh * G + h] = lse_n;
+        } else {
+          const int pidx = __ldg(p.part_begin + item.r) + item.local;
+          p.part_o[((int64_t)pidx * G) * D + e] = ov;
+          if ((e - h * D) == 0) p.part_lse[(int64_t)pidx * G + h] = lse_n;
+        }
+      }
+    } else if (tid == 0) {
+      atomicOr(&p.ctrl[CTRL_ERR], PKV_DEV_BAD_PAGE);
+      atomicOr(p.dev_status, PKV_DEV_BAD_PAGE);
+    }
+  }
+}
+
+template <typename T, int D, int G>
+cudaError_t launch_dec(const AttnArgs& a, cudaStream_t s) {
+  using C = DCfg<T, D, G>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(decode_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const CUtensorMapDataType dt = std::is_same<T, float>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                  : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int box_rows = a.P >= BT ? BT : a.P;
+  CUtensorMap mk, mv;
+  if (!make_map_boxed(&mk, a.k_cache, dt, C::ELT, D, a.Hkv, (int64_t)a.num_pages * a.P, C::ATOM_ELEMS, box_rows) ||
+      !make_map_boxed(&mv, a.v_cache, dt, C::ELT, D, a.Hkv, (int64_t)a.num_pages * a.P, C::ATOM_ELEMS, box_rows))
+    return cudaErrorInvalidValue;
+  DecParams p;
+  p.cu = a.cu;
+  p.kv_lens = a.kv_lens;
+  p.page_tables = a.page_tables;
+  p.q = a.q;
+  p.B = a.B;
+  p.T = a.T;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.P = a.P;
+  p.num_pages = a.num_pages;
+  p.max_pages = a.max_pages;
+  p.scale_log2 = a.scale * LOG2E;
+  p.out = a.out;
+  p.lse = a.lse;
+  p.ctrl = (int32_t*)(a.ws + a.lay.ctrl);
+  p.item_begin = (const int32_t*)(a.ws + a.lay.row_item_begin);
+  p.part_begin = (const int32_t*)(a.ws + a.lay.row_part_begin);
+  p.part_o = (float*)(a.ws + a.lay.part_o);
+  p.part_lse = (float*)(a.ws + a.lay.part_lse);
+  p.dev_status = a.dev_status;
+  decode_kernel<T, D, G><<<a.num_sms * CTAS_PER_SM, NTHREADS, C::SMEM, s>>>(mk, mv, p);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_dec_g(const AttnArgs& a, cudaStream_t s) {
+  switch (a.Hq / a.Hkv) {
+    case 1: return launch_dec<T, D, 1>(a, s);
+    case 2: return launch_dec<T, D, 2>(a, s);
+    case 4: return launch_dec<T, D, 4>(a, s);
+    case 8: return launch_dec<T, D, 8>(a, s);
+    case 16: return launch_dec<T, D, 16>(a, s);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+template <typename T>
+cudaError_t launch_dec_d(const AttnArgs& a, cudaStream_t s) {
+  return a.D == 64 ? launch_dec_g<T, 64>(a, s) : launch_dec_g<T, 128>(a, s);
+}
+
+}  // namespace
+
+bool decode_supported(int dtype, int D, int P) {
+  (void)dtype;
+  if (D != 64 && D != 128) return false;
+  if (P % BT == 0) return true;
+  return P >= 8 && P % 8 == 0 && BT % P == 0;
+}
+
+cudaError_t launch_decode(const AttnArgs& a, cudaStream_t s) {
+  if (!decode_supported(a.dtype, a.D, a.P)) return cudaErrorNotSupported;
+  KernelTimer timer("decode", s);
+  switch (a.dtype) {
+    case PKV_F32: return launch_dec_d<float>(a, s);
+    case PKV_F16: return launch_dec_d<__half>(a, s);
+    default: return launch_dec_d<__nv_bfloat16>(a, s);
+  }
+}
+
+}  // namespace pkv

@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libpagedkv.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -98,6 +99,13 @@ cudaError_t launch_combine(const AttnArgs& a, cudaStream_t s);
 // Returns cudaErrorNotSupported when the shape has no tensor-core path.
 cudaError_t launch_prefill_tc(const AttnArgs& a, cudaStream_t s);
 bool prefill_tc_supported(int dtype, int D, int P);
+// TMA-staged decode kernel for single rows (cudaErrorNotSupported if the shape has none).
+cudaError_t launch_decode(const AttnArgs& a, cudaStream_t s);
+bool decode_supported(int dtype, int D, int P);
+
+// TMA tensor map of a contiguous [rows, heads, D] tensor, 128-byte swizzled boxes.
+bool make_map_boxed(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elt, int D, int heads,
+                    int64_t rows, int box_cols, int box_rows);
 
 // workers of the row kernel (for the split policy)
 int rows_kernel_workers(int num_sms);

@@ -487,34 +487,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 // --------------------------------------------------------------------------- host
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static std::once_flag once;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
-  });
-  return fn;
-}
-
-// 3-D view [rows, heads, D] of a contiguous tensor, 64-column boxes of `box_rows` rows.
-bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int D, int heads, int64_t rows,
-              int box_rows) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D, typename T>
 cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
   using C = Cfg<D>;
@@ -528,9 +500,9 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
       std::is_same<T, __nv_bfloat16>::value ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap mq, mk, mv;
   const int box = a.P >= BN ? BN : a.P;
-  if (!make_map(&mq, a.q, dt, D, a.Hq, a.T, BM) ||
-      !make_map(&mk, a.k_cache, dt, D, a.Hkv, (int64_t)a.num_pages * a.P, box) ||
-      !make_map(&mv, a.v_cache, dt, D, a.Hkv, (int64_t)a.num_pages * a.P, box))
+  if (!make_map_boxed(&mq, a.q, dt, 2, D, a.Hq, a.T, 64, BM) ||
+      !make_map_boxed(&mk, a.k_cache, dt, 2, D, a.Hkv, (int64_t)a.num_pages * a.P, 64, box) ||
+      !make_map_boxed(&mv, a.v_cache, dt, 2, D, a.Hkv, (int64_t)a.num_pages * a.P, 64, box))
     return cudaErrorInvalidValue;
   TcParams p;
   p.cu = a.cu;
