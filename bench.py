@@ -45,6 +45,25 @@ DESCRIPTIONS = {
 }
 
 
+def load_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, or None
+    when there is none or the kernel's source changed since the capture."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:12]
+    return int(rec["bytes"]) if h == rec["sha256_12"] else None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -76,6 +95,25 @@ def tick_work(w):
                 prefill_flops=prefill_flops, prefill_bytes=prefill_bytes, append_bytes=append_bytes)
 
 
+def kernel_roofline(kernel, ktimes, work, peaks, workload):
+    """Achieved vs peak for one kernel: algorithmic work per launch / average
+    device time per launch (CUDA events on the launch stream)."""
+    n, total_ms = ktimes[kernel]
+    avg_s = total_ms / n / 1000.0
+    traffic = load_traffic(kernel) if workload == "mixed_tick" else None
+    if kernel == "prefill_tc":
+        ach = work["prefill_flops"] / avg_s / 1e12
+        return {"kernel": kernel, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": traffic,
+                "algorithmic_per_launch": work["prefill_flops"], "avg_launch_us": avg_s * 1e6,
+                "peak_source": peaks["source"] + " bf16 burst"}
+    nbytes = {"kv_append": work["append_bytes"]}.get(kernel, work["decode_bytes"])
+    ach = nbytes / avg_s / 1e9
+    return {"kernel": kernel, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": ach / peaks["hbm_gbs"], "traffic": traffic, "algorithmic_per_launch": nbytes,
+            "avg_launch_us": avg_s * 1e6, "peak_source": peaks["source"] + " copy bandwidth"}
+
+
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 
@@ -84,15 +122,16 @@ class ClockSampler:
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index=0):
+    def __init__(self, index=0, period_ms=50):
         self.index = index
+        self.period_ms = period_ms
         self.proc = None
         self.lines = []
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -237,7 +276,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mixed_tick", choices=list(W.WORKLOADS))
@@ -279,6 +318,9 @@ def main():
         binding.kv_append(kn, vn, slots, kc, vc)
         binding.paged_attention(q, cu, kv, pt, kc, vc, w.scale, w.max_kv_len, out=out, lse=lse, workspace=ws)
 
+    clk = ClockSampler(local)
+    clk.__enter__()
+    time.sleep(0.3)   # let nvidia-smi start sampling before the GPU work
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -293,16 +335,15 @@ def main():
     # pass A: the headline number (no per-kernel events)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     binding.set_kernel_timing(False)
-    with ClockSampler(local) as clk:
-        barrier()
-        torch.cuda.synchronize()
-        for a, b in ev:
-            flush.zero_()
-            a.record(stream)
-            step()
-            b.record(stream)
-        torch.cuda.synchronize()
-        barrier()
+    barrier()
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier()
     ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     if world > 1:
         import torch.distributed as dist
@@ -362,6 +403,7 @@ def main():
         t = torch.tensor([e2e_avg], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_avg = float(t.item())
+    clk.__exit__(None, None, None)
     h2d = meta_bytes + sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v))
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
 
@@ -378,18 +420,8 @@ def main():
     roof = None
     if dom is not None:
         avg_s = ktimes[dom][1] / ktimes[dom][0] / 1000.0
-        if dom == "prefill_tc":
-            ach = work["prefill_flops"] / avg_s / 1e12
-            roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": None,
-                    "algorithmic_per_launch": work["prefill_flops"]}
-        else:
-            nbytes = {"rows": work["decode_bytes"], "decode_tc": work["decode_bytes"],
-                      "kv_append": work["append_bytes"]}.get(dom, work["decode_bytes"])
-            ach = nbytes / avg_s / 1e9
-            roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": ach / peaks["hbm_gbs"], "traffic": None, "algorithmic_per_launch": nbytes}
-        roof["peak_source"] = peaks["source"]
+        roof = kernel_roofline(dom, ktimes, work, peaks, args.workload)
+    roof_decode = kernel_roofline("decode", ktimes, work, peaks, args.workload) if "decode" in ktimes else None
     decode_k = "decode" if "decode" in ktimes else ("rows" if "rows" in ktimes else None)
     decode_gbs = None
     if decode_k and work["decode_bytes"]:
@@ -408,6 +440,7 @@ def main():
                    "tokens_per_step": T, "l2": "flushed between steps (512 MB write, outside the step events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "roofline": roof,
+        "roofline_decode": roof_decode,
         "decode_hbm_gbs": decode_gbs,
         "kernels": per_kernel,
         "cpu_baseline": cpu,
