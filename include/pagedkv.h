@@ -229,6 +229,10 @@ int pkv_paged_attention_no_alloc(const void* q, const int32_t* cu_seqlens_q, con
 /* Human-readable text for a pkv_status code (static storage). */
 const char* pkv_status_string(int status);
 
+/* Text of the CUDA error behind the calling thread's last PKV_E_CUDA
+ * (thread-local storage, valid until that thread's next failing call). */
+const char* pkv_last_error(void);
+
 /* Waits for `stream`, then returns in *code the OR of the PKV_DEV_* bits set
  * on the current device since the last call, and clears them. */
 int pkv_get_device_status(int32_t* code, pkv_stream_t stream);

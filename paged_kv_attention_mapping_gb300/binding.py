@@ -30,13 +30,15 @@ EXPORTED = (
     "pkv_set_kernel_timing",
     "pkv_kernel_times",
     "pkv_version",
+    "pkv_last_error",
 )
 
 
 class PagedKVError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        detail = f"; {lib().pkv_last_error().decode()}" if status == -8 else ""
+        super().__init__(f"{where}: {status_string(status)} (status {status}){detail}")
 
 
 class CacheDesc(ctypes.Structure):
@@ -78,6 +80,8 @@ def lib():
     L.pkv_set_kernel_timing.restype = ctypes.c_int
     L.pkv_kernel_times.argtypes = [ctypes.POINTER(ctypes.c_char_p), P32, ctypes.POINTER(ctypes.c_double), i32]
     L.pkv_kernel_times.restype = ctypes.c_int
+    L.pkv_last_error.argtypes = []
+    L.pkv_last_error.restype = ctypes.c_char_p
     L.pkv_version.argtypes = []
     L.pkv_version.restype = ctypes.c_char_p
     _lib = L

@@ -2,6 +2,7 @@
 // on the caller's stream, the device status word and kernel timing.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <string.h>
 
 #include <mutex>
@@ -89,9 +90,19 @@ KernelTimer::~KernelTimer() {
   if (slot_ < (int)g_recs.size()) cudaEventRecord(g_recs[slot_].b, s_);
 }
 
+static thread_local char g_last_error[256] = "no error";
+
+// Record the text of a failed CUDA call; returns PKV_E_CUDA.
+int cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
+  return PKV_E_CUDA;
+}
+
 }  // namespace pkv
 
 using namespace pkv;
+
+extern "C" const char* pkv_last_error(void) { return g_last_error; }
 
 // ---------------------------------------------------------------------------
 // C ABI
@@ -140,7 +151,7 @@ extern "C" int pkv_kv_append(const void* k, const void* v, const int64_t* slot_m
   if (!f) return PKV_E_CUDA;
   if (!f->ok) return PKV_E_DEVICE;
   cudaError_t e = launch_append(k, v, slot_mapping, num_tokens, k_cache, v_cache, *cache, (cudaStream_t)stream);
-  return e == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "kv_append");
 }
 
 static bool head_dim_supported(int d) { return d == 64 || d == 128; }
@@ -211,7 +222,7 @@ extern "C" int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, c
   pa.lay = lay;
   pa.dev_status = f->status;
   cudaError_t e = launch_plan(pa, s);
-  if (e != cudaSuccess) return PKV_E_CUDA;
+  if (e != cudaSuccess) return cuda_fail(e, "plan");
 
   AttnArgs aa{};
   aa.q = q;
@@ -238,12 +249,12 @@ extern "C" int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, c
   aa.dev_status = f->status;
   if (tc) {
     e = launch_prefill_tc(aa, s);
-    if (e != cudaSuccess) return PKV_E_CUDA;
+    if (e != cudaSuccess) return cuda_fail(e, "prefill_tc");
   }
   e = decode_supported(aa.dtype, aa.D, aa.P) ? launch_decode(aa, s) : launch_rows(aa, s);
-  if (e != cudaSuccess) return PKV_E_CUDA;
+  if (e != cudaSuccess) return cuda_fail(e, "decode");
   e = launch_combine(aa, s);
-  if (e != cudaSuccess) return PKV_E_CUDA;
+  if (e != cudaSuccess) return cuda_fail(e, "combine");
   return PKV_OK;
 }
 

@@ -12,6 +12,7 @@ namespace pkv {
 // ---------------------------------------------------------------------------
 // device status word (one per device, in pkv_api.cu)
 int32_t* device_status_ptr();  // device address of the status word on the current device
+int cuda_fail(cudaError_t e, const char* where);  // records the error text, returns PKV_E_CUDA
 
 // ---------------------------------------------------------------------------
 // kernel timing hooks (pkv_api.cu). A KernelTimer brackets one launch with
@@ -99,6 +100,9 @@ cudaError_t launch_combine(const AttnArgs& a, cudaStream_t s);
 // Returns cudaErrorNotSupported when the shape has no tensor-core path.
 cudaError_t launch_prefill_tc(const AttnArgs& a, cudaStream_t s);
 bool prefill_tc_supported(int dtype, int D, int P);
+// Two query tiles (two q heads of one GQA group) per CTA; needs an even group size and scale > 0.
+bool prefill_tc2_supported(int dtype, int D, int P, int Hq, int Hkv, float scale);
+cudaError_t launch_prefill_tc2(const AttnArgs& a, cudaStream_t s);
 // TMA-staged decode kernel for single rows (cudaErrorNotSupported if the shape has none).
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t s);
 bool decode_supported(int dtype, int D, int P);

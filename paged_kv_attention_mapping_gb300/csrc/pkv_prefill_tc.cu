@@ -360,8 +360,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
-          tmem_ld32(tmem + lrow + TMEM_S + sb * BN + c * 32, r);
-          tmem_wait_ld();
+          tmem_ld32_wait(tmem + lrow + TMEM_S + sb * BN + c * 32, r);
 #pragma unroll
           for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
         }
@@ -402,13 +401,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t r[32];
-            tmem_ld32(tmem + lrow + TMEM_O + c * 32, r);
-            tmem_wait_ld();
+            tmem_ld32_wait(tmem + lrow + TMEM_O + c * 32, r);
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(tmem + lrow + TMEM_O + c * 32, r);
+            tmem_st32_wait(tmem + lrow + TMEM_O + c * 32, r);
           }
-          tmem_wait_st();
         }
         m_run = m_new;
         float lsum = 0.f;
@@ -445,8 +442,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
-          tmem_ld32(tmem + lrow + TMEM_O + c * 32, r);
-          tmem_wait_ld();
+          tmem_ld32_wait(tmem + lrow + TMEM_O + c * 32, r);
           if (!store) continue;
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
@@ -536,6 +532,7 @@ bool prefill_tc_supported(int dtype, int D, int P) {
 
 cudaError_t launch_prefill_tc(const AttnArgs& a, cudaStream_t s) {
   if (!prefill_tc_supported(a.dtype, a.D, a.P)) return cudaErrorNotSupported;
+  if (prefill_tc2_supported(a.dtype, a.D, a.P, a.Hq, a.Hkv, a.scale)) return launch_prefill_tc2(a, s);
   KernelTimer timer("prefill_tc", s);
   if (a.dtype == PKV_BF16) return a.D == 64 ? launch_tc<64, __nv_bfloat16>(a, s) : launch_tc<128, __nv_bfloat16>(a, s);
   return a.D == 64 ? launch_tc<64, __half>(a, s) : launch_tc<128, __half>(a, s);

@@ -1,0 +1,558 @@
+// Prefill-chunk attention on tcgen05, two query tiles per CTA.
+//
+// Same problem as pkv_prefill_tc.cu (a chunk of new tokens after a cached
+// prefix: whole prefix visible, causal inside the chunk; llm-serving-engine
+// README, engine step trace "_step_prefill"; Helios README, "Paged attention"),
+// arranged so that the tensor core always has the other tile's work while one
+// tile is in its softmax. A work tile is (sequence, 128 query rows, two q heads
+// of the same GQA group): both query tiles read the same K/V tiles and have the
+// same causal mask, so every K/V tile fetched by TMA feeds four MMAs.
+//
+//   warp 0      TMA producer: Q of both heads, then K_j, V_j into a 3-slot ring
+//               (V rows past kv_len zeroed in the last tile)
+//   warp 1      TMEM owner (512 columns) and MMA issuer:
+//               S_w = Q_w K_j^T  (w = 0, 1; TMEM columns 128 w),
+//               O_w += P_w V_{j-1} (TMEM columns 256 + 128 w)
+//   warps 2-5   softmax of query tile 0, one thread per row
+//   warps 6-9   softmax of query tile 1
+// The softmax copies its S row to registers and frees the S buffer at once, so
+// the next QK^T into it can start; a masked max pass (only for tiles on the
+// causal diagonal) and one exp pass (scale folded into an FFMA, raw ex2) write
+// P in bf16/fp16 to shared memory (128-byte swizzled K-major, PV's A operand).
+// O is rescaled in TMEM only when a row's max grows by more than 2^8.
+// Every mbarrier wait is bounded (PKV_DEV_TIMEOUT); TMEM accesses are
+// warp-uniform.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "pkv_common.cuh"
+#include "pkv_internal.h"
+#include "pkv_sm100.cuh"
+
+namespace pkv {
+using namespace sm100;
+
+namespace {
+
+constexpr int BM = TC_BM;
+constexpr int BN = TC_BN;
+constexpr int NWG = 2;
+constexpr int NTHREADS = (2 + 4 * NWG) * 32;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float RESCALE_LOG2 = 8.f;
+
+struct Params2 {
+  const int32_t* cu;
+  const int32_t* kv_lens;
+  const int32_t* page_tables;
+  int B, T, Hq, Hkv, P, num_pages, max_pages;
+  float scale_log2;  // > 0
+  void* out;
+  float* lse;
+  int32_t* ctrl;
+  const int2* pairs;
+  int32_t* dev_status;
+};
+
+struct Tile2 {
+  int valid;
+  int b, h, kvh, row0, nr, L, p_first, n_kv, j_mask, zero_from;
+};
+
+template <int D>
+struct Cfg2 {
+  static constexpr int HALVES = D / 64;
+  static constexpr int NSLOT = D == 128 ? 3 : 4;
+  static constexpr uint32_t Q_BYTES = BM * D * 2;       // one query tile
+  static constexpr uint32_t SLOT_BYTES = BN * D * 2;
+  static constexpr uint32_t P_BYTES = BM * BN * 2;      // one P tile
+  static constexpr uint32_t SMEM = NWG * Q_BYTES + NSLOT * SLOT_BYTES + NWG * P_BYTES + 1024;
+  static_assert(SMEM <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ bool wait2(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* ctrl,
+                                      int32_t* dev_status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > 2000000000ull || it > (1u << 28)) {
+        *abort_flag = 1;
+        atomicOr(&ctrl[CTRL_ERR], PKV_DEV_TIMEOUT);
+        atomicOr(dev_status, PKV_DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    prefill_tc2_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                       const __grid_constant__ CUtensorMap mv, Params2 p) {
+  using C = Cfg2<D>;
+  constexpr int NS = C::NSLOT;
+  constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  unsigned char* sQ = sm;                                   // [NWG][Q tile]
+  unsigned char* sRing = sQ + NWG * C::Q_BYTES;             // [NS][slot]
+  unsigned char* sP = sRing + NS * C::SLOT_BYTES;           // [NWG][P tile]
+
+  __shared__ __align__(8) uint64_t bar_q, bar_full[NS], bar_empty[NS], bar_sfull[NWG], bar_sfree[NWG],
+      bar_pfull[NWG], bar_odone[NWG], bar_vfix, bar_drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ Tile2 s_tile;
+  __shared__ volatile int s_abort;
+  __shared__ int s_bad;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    mbar_init(&bar_q, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int w = 0; w < NWG; ++w) {
+      mbar_init(&bar_sfull[w], 1);
+      mbar_init(&bar_sfree[w], 128);
+      mbar_init(&bar_pfull[w], 128);
+      mbar_init(&bar_odone[w], 1);
+    }
+    mbar_init(&bar_vfix, 1);
+    mbar_init(&bar_drain, 1);
+    fence_mbar_init();
+    s_abort = 0;
+    tma_prefetch_desc(&mq);
+    tma_prefetch_desc(&mk);
+    tma_prefetch_desc(&mv);
+  }
+  if (warp == 1) tmem_alloc(&s_tmem, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int hpairs = p.Hq / 2;
+  const int n_tiles = *(volatile int32_t*)&p.ctrl[CTRL_N_PAIRS] * hpairs;
+  const int g = p.Hq / p.Hkv;
+
+  uint32_t ring = 0;                   // producer / MMA
+  uint32_t s_use[NWG] = {0, 0};        // MMA: QK issued per S buffer
+  uint32_t p_use[NWG] = {0, 0};        // MMA: P consumed per group
+  uint32_t my_s = 0, my_o = 0;         // softmax thread: S waits, PV waits of its group
+  uint32_t tile_cnt = 0;
+  uint32_t fills[NS];
+#pragma unroll
+  for (int s = 0; s < NS; ++s) fills[s] = 0;
+
+  for (;;) {
+    if (tid == 0) {
+      Tile2 ti;
+      ti.valid = 0;
+      const int t = atomicAdd(&p.ctrl[CTRL_TILE_NEXT], 1);
+      if (t < n_tiles && !s_abort) {
+        const int2 pr = p.pairs[t / hpairs];
+        ti.b = pr.x;
+        ti.h = (t % hpairs) * 2;
+        ti.kvh = ti.h / g;
+        const int c0 = p.cu[ti.b];
+        const int qlen = p.cu[ti.b + 1] - c0;
+        ti.L = p.kv_lens[ti.b];
+        const int q0 = pr.y * BM;
+        ti.row0 = c0 + q0;
+        ti.nr = min(BM, qlen - q0);
+        ti.p_first = ti.L - qlen + q0;
+        const int p_last = ti.p_first + ti.nr - 1;
+        ti.n_kv = (p_last + 1 + BN - 1) / BN;
+        ti.j_mask = (ti.p_first + 1) / BN;
+        ti.zero_from = min(BN, ti.L - (ti.n_kv - 1) * BN);
+        ti.valid = 1;
+      }
+      s_tile = ti;
+      s_bad = 0;
+    }
+    __syncthreads();
+    const Tile2 ti = s_tile;
+    if (!ti.valid) break;
+    const int32_t* pt = p.page_tables + (int64_t)ti.b * p.max_pages;
+
+    if (warp == 0) {
+      // ------------------------------------------------------------- producer
+      bool ok = true;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar_q, NWG * C::Q_BYTES);
+#pragma unroll
+        for (int w = 0; w < NWG; ++w)
+#pragma unroll
+          for (int hf = 0; hf < C::HALVES; ++hf)
+            tma_load_3d(sQ + w * C::Q_BYTES + hf * BM * 128, &mq, &bar_q, hf * 64, ti.h + w, ti.row0);
+      }
+      const int n_pages_seq = (ti.L + p.P - 1) / p.P;
+      for (int j = 0; j < ti.n_kv && ok; ++j) {
+        for (int kv = 0; kv < 2 && ok; ++kv) {
+          const uint32_t slot = ring % NS, round = ring / NS;
+          ++ring;
+          if (!__all_sync(0xffffffffu,
+                          wait2(&bar_empty[slot], (round & 1) ^ 1, &s_abort, p.ctrl, p.dev_status))) {
+            ok = false;
+            break;
+          }
+          unsigned char* dst = sRing + slot * C::SLOT_BYTES;
+          const CUtensorMap* map = kv == 0 ? &mk : &mv;
+          if (lane == 0) {
+            if (p.P >= BN) {
+              const int lp = (j * BN) / p.P;
+              const int off = (j * BN) - lp * p.P;
+              const int page = pt[lp];
+              if (page < 0 || page >= p.num_pages) {
+                atomicOr(&s_bad, 1);
+                mbar_arrive(&bar_full[slot]);
+              } else {
+                mbar_arrive_expect_tx(&bar_full[slot], C::SLOT_BYTES);
+#pragma unroll
+                for (int hf = 0; hf < C::HALVES; ++hf)
+                  tma_load_3d(dst + hf * BN * 128, map, &bar_full[slot], hf * 64, ti.kvh, page * p.P + off);
+              }
+            } else {
+              const int per = BN / p.P;
+              const int lp0 = j * per;
+              const int cnt = min(per, n_pages_seq - lp0);
+              bool bad = false;
+              for (int pp = 0; pp < cnt; ++pp) {
+                const int page = pt[lp0 + pp];
+                bad |= page < 0 || page >= p.num_pages;
+              }
+              if (bad) {
+                atomicOr(&s_bad, 1);
+                mbar_arrive(&bar_full[slot]);
+              } else {
+                mbar_arrive_expect_tx(&bar_full[slot], (uint32_t)cnt * p.P * D * 2);
+                for (int pp = 0; pp < cnt; ++pp) {
+                  const int page = pt[lp0 + pp];
+#pragma unroll
+                  for (int hf = 0; hf < C::HALVES; ++hf)
+                    tma_load_3d(dst + hf * BN * 128 + pp * p.P * 128, map, &bar_full[slot], hf * 64, ti.kvh,
+                                page * p.P);
+                }
+              }
+            }
+          }
+          fills[slot] += 1;
+          if (kv == 1 && j == ti.n_kv - 1) {
+            if (ti.zero_from < BN) {
+              if (!__all_sync(0xffffffffu, wait2(&bar_full[slot], round & 1, &s_abort, p.ctrl, p.dev_status))) {
+                ok = false;
+                break;
+              }
+              for (int hf = 0; hf < C::HALVES; ++hf) {
+                uint4* base = (uint4*)(dst + hf * BN * 128);
+                for (int e = ti.zero_from * 8 + lane; e < BN * 8; e += 32) base[e] = make_uint4(0, 0, 0, 0);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+            }
+            if (lane == 0) mbar_arrive(&bar_vfix);
+          }
+        }
+      }
+      if (!ok && lane == 0) {
+        for (int s = 0; s < NS; ++s)
+          if (fills[s] > 0) mbar_wait(&bar_full[s], (fills[s] - 1) & 1, 500000000ull);
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        const uint32_t id_qk = idesc_f16(BM, BN, BF16, false);
+        const uint32_t id_pv = idesc_f16(BM, D, BF16, true);
+        const uint32_t base = ring;
+        bool ok = wait2(&bar_q, tile_cnt & 1, &s_abort, p.ctrl, p.dev_status);
+        tc_fence_after();
+        // per KV tile j, for each query tile w: S_w = Q_w K_j^T, then O_w += P_w V_{j-1}
+        // (both wait for the end of w's softmax of tile j-1, so the other query
+        // tile's MMAs keep the tensor core busy meanwhile)
+        for (int j = 0; j <= ti.n_kv && ok; ++j) {
+          const bool qk = j < ti.n_kv, pv = j > 0;
+          const uint32_t ik = base + 2 * j, iv = base + 2 * j - 1;
+          const uint32_t kslot = ik % NS, vslot = iv % NS;
+          if (qk && !wait2(&bar_full[kslot], (ik / NS) & 1, &s_abort, p.ctrl, p.dev_status)) {
+            ok = false;
+            break;
+          }
+          if (pv) {
+            if (!wait2(&bar_full[vslot], (iv / NS) & 1, &s_abort, p.ctrl, p.dev_status) ||
+                (j == ti.n_kv && !wait2(&bar_vfix, tile_cnt & 1, &s_abort, p.ctrl, p.dev_status))) {
+              ok = false;
+              break;
+            }
+          }
+          const uint32_t k_base = smem_u32(sRing + kslot * C::SLOT_BYTES);
+          const uint32_t v_base = smem_u32(sRing + vslot * C::SLOT_BYTES);
+#pragma unroll
+          for (int w = 0; w < NWG; ++w) {
+            if (qk) {
+              if (!wait2(&bar_sfree[w], (s_use[w] & 1) ^ 1, &s_abort, p.ctrl, p.dev_status)) {
+                ok = false;
+                break;
+              }
+              ++s_use[w];
+              tc_fence_after();
+              const uint32_t q_base = smem_u32(sQ + w * C::Q_BYTES);
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk / 4) * BM * 128 + (kk % 4) * 32;
+                const uint32_t offk = (kk / 4) * BN * 128 + (kk % 4) * 32;
+                mma_f16_ss(tmem + w * 128, smem_desc(q_base + off, 16, 1024, LAYOUT_SW128),
+                           smem_desc(k_base + offk, 16, 1024, LAYOUT_SW128), id_qk, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(&bar_sfull[w]);
+            }
+            if (pv) {
+              if (!wait2(&bar_pfull[w], p_use[w] & 1, &s_abort, p.ctrl, p.dev_status)) {
+                ok = false;
+                break;
+              }
+              ++p_use[w];
+              tc_fence_after();
+              const uint32_t p_base = smem_u32(sP + w * C::P_BYTES);
+#pragma unroll
+              for (int kk = 0; kk < BN / 16; ++kk) {
+                const uint64_t ad = smem_desc(p_base + (kk / 4) * BM * 128 + (kk % 4) * 32, 16, 1024, LAYOUT_SW128);
+                const uint64_t bd = smem_desc(v_base + kk * 16 * 128, BN * 128, 1024, LAYOUT_SW128);
+                mma_f16_ss(tmem + 256 + w * 128, ad, bd, id_pv, (j > 1 || kk > 0) ? 1u : 0u);
+              }
+              mma_commit(&bar_odone[w]);
+            }
+          }
+          if (!ok) break;
+          if (qk) mma_commit(&bar_empty[kslot]);
+          if (pv) mma_commit(&bar_empty[vslot]);
+        }
+      }
+      ring += 2 * ti.n_kv;
+    } else {
+      // --------------------------------------------------------------- softmax
+      const int w = (warp - 2) >> 2;                // query tile of this warpgroup
+      const int qq = warp & 3;                      // TMEM lane quarter of this warp
+      const int i = qq * 32 + lane;                 // row within the tile
+      const uint32_t lrow = (uint32_t)(qq * 32) << 16;
+      const uint32_t s_col = w * 128, o_col = 256 + w * 128;
+      const int p_i = min(ti.p_first + i, ti.L - 1);
+      const float sc = p.scale_log2;
+      unsigned char* prow = sP + w * C::P_BYTES + i * 128;
+      float m_run = -INFINITY, l_run = 0.f;
+      bool ok = true;
+      for (int j = 0; j < ti.n_kv && ok; ++j) {
+        if (!__all_sync(0xffffffffu, wait2(&bar_sfull[w], my_s & 1, &s_abort, p.ctrl, p.dev_status))) {
+          ok = false;
+          break;
+        }
+        ++my_s;
+        tc_fence_after();
+        const bool masked = j >= ti.j_mask;
+        const int lim = p_i - j * BN;               // keys with index <= lim are visible
+        // pass 1: row max of the raw scores (scale > 0 keeps the order)
+        float mx[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32_wait(tmem + lrow + s_col + c * 32, r);
+          if (masked) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              mx[e & 7] = fmaxf(mx[e & 7], c * 32 + e <= lim ? __uint_as_float(r[e]) : -INFINITY);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(r[e]));
+          }
+        }
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sc;
+        const bool first = j == 0;
+        const bool grow = first || mt > m_run + RESCALE_LOG2;
+        const float m_new = grow ? fmaxf(mt, m_run) : m_run;
+        if (!first) {
+          // PV_{j-1} must be done before P is overwritten or O rescaled
+          if (!__all_sync(0xffffffffu, wait2(&bar_odone[w], my_o & 1, &s_abort, p.ctrl, p.dev_status))) {
+            ok = false;
+            break;
+          }
+          ++my_o;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, grow)) {
+            const float alpha = grow ? ex2(m_run - m_new) : 1.f;
+            l_run *= alpha;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32_wait(tmem + lrow + o_col + c * 32, r);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+              tmem_st32_wait(tmem + lrow + o_col + c * 32, r);
+            }
+          }
+        }
+        m_run = m_new;
+        // pass 2: P = exp2(scale * S - m) in 16-bit into shared memory, row sum in fp32
+        const float neg_m = -m_run;
+        float ls[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32_wait(tmem + lrow + s_col + c * 32, r);
+          if (c == BN / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(&bar_sfree[w]);             // S fully read: the next Q K^T may overwrite it
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {          // 4 x 8 keys = one 16-byte chunk of P each
+            uint32_t wv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int k0 = q4 * 8 + 2 * e;
+              float a = ex2(fmaf(__uint_as_float(r[k0]), sc, neg_m));
+              float b = ex2(fmaf(__uint_as_float(r[k0 + 1]), sc, neg_m));
+              if (masked) {
+                a = c * 32 + k0 <= lim ? a : 0.f;
+                b = c * 32 + k0 + 1 <= lim ? b : 0.f;
+              }
+              ls[(2 * e) & 7] += a;
+              ls[(2 * e + 1) & 7] += b;
+              wv[e] = pack_h2<T>(a, b);
+            }
+            const int ch = c * 4 + q4;              // 16-byte chunk index along the 128 keys
+            const int hf = ch >> 3, c8 = ch & 7;
+            *reinterpret_cast<uint4*>(prow + hf * BM * 128 + ((c8 ^ (i & 7)) << 4)) =
+                make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          }
+        }
+        l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bar_pfull[w]);
+      }
+      if (ok) ok = __all_sync(0xffffffffu, wait2(&bar_odone[w], my_o & 1, &s_abort, p.ctrl, p.dev_status));
+      ++my_o;
+      if (ok) ok = __all_sync(0xffffffffu, wait2(&bar_vfix, tile_cnt & 1, &s_abort, p.ctrl, p.dev_status));
+      tc_fence_after();
+      if (ok) {
+        const bool store = i < ti.nr && !s_bad;
+        const float inv = 1.f / l_run;
+        T* dst = (T*)p.out + ((int64_t)(ti.row0 + i) * p.Hq + ti.h + w) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32_wait(tmem + lrow + o_col + c * 32, r);
+          if (!store) continue;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 pk;
+            pk.x = pack_h2<T>(__uint_as_float(r[v * 8 + 0]) * inv, __uint_as_float(r[v * 8 + 1]) * inv);
+            pk.y = pack_h2<T>(__uint_as_float(r[v * 8 + 2]) * inv, __uint_as_float(r[v * 8 + 3]) * inv);
+            pk.z = pack_h2<T>(__uint_as_float(r[v * 8 + 4]) * inv, __uint_as_float(r[v * 8 + 5]) * inv);
+            pk.w = pack_h2<T>(__uint_as_float(r[v * 8 + 6]) * inv, __uint_as_float(r[v * 8 + 7]) * inv);
+            *reinterpret_cast<uint4*>(dst + c * 32 + v * 8) = pk;
+          }
+        }
+        if (store && p.lse) p.lse[(int64_t)(ti.row0 + i) * p.Hq + ti.h + w] = (m_run + __log2f(l_run)) * LN2;
+        if (i == 0 && w == 0 && s_bad) {
+          atomicOr(&p.ctrl[CTRL_ERR], PKV_DEV_BAD_PAGE);
+          atomicOr(p.dev_status, PKV_DEV_BAD_PAGE);
+        }
+      }
+      tc_fence_before();
+    }
+    ++tile_cnt;
+    __syncthreads();
+    if (s_abort) break;
+  }
+
+  if (warp == 1) {
+    if (lane == 0) {
+      mma_commit(&bar_drain);
+      mbar_wait(&bar_drain, 0, 500000000ull);
+    }
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+template <int D, typename T>
+cudaError_t launch2(const AttnArgs& a, cudaStream_t s) {
+  using C = Cfg2<D>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(prefill_tc2_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const CUtensorMapDataType dt =
+      std::is_same<T, __nv_bfloat16>::value ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap mq, mk, mv;
+  const int box = a.P >= BN ? BN : a.P;
+  if (!make_map_boxed(&mq, a.q, dt, 2, D, a.Hq, a.T, 64, BM) ||
+      !make_map_boxed(&mk, a.k_cache, dt, 2, D, a.Hkv, (int64_t)a.num_pages * a.P, 64, box) ||
+      !make_map_boxed(&mv, a.v_cache, dt, 2, D, a.Hkv, (int64_t)a.num_pages * a.P, 64, box))
+    return cudaErrorInvalidValue;
+  Params2 p;
+  p.cu = a.cu;
+  p.kv_lens = a.kv_lens;
+  p.page_tables = a.page_tables;
+  p.B = a.B;
+  p.T = a.T;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.P = a.P;
+  p.num_pages = a.num_pages;
+  p.max_pages = a.max_pages;
+  p.scale_log2 = a.scale * LOG2E;
+  p.out = a.out;
+  p.lse = a.lse;
+  p.ctrl = (int32_t*)(a.ws + a.lay.ctrl);
+  p.pairs = (const int2*)(a.ws + a.lay.tc_pairs);
+  p.dev_status = a.dev_status;
+  prefill_tc2_kernel<D, T><<<a.num_sms, NTHREADS, C::SMEM, s>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool prefill_tc2_supported(int dtype, int D, int P, int Hq, int Hkv, float scale) {
+  if (!prefill_tc_supported(dtype, D, P)) return false;
+  return (Hq / Hkv) % 2 == 0 && scale > 0.f;
+}
+
+cudaError_t launch_prefill_tc2(const AttnArgs& a, cudaStream_t s) {
+  KernelTimer timer("prefill_tc", s);
+  if (a.dtype == PKV_BF16) return a.D == 64 ? launch2<64, __nv_bfloat16>(a, s) : launch2<128, __nv_bfloat16>(a, s);
+  return a.D == 64 ? launch2<64, __half>(a, s) : launch2<128, __half>(a, s);
+}
+
+}  // namespace pkv

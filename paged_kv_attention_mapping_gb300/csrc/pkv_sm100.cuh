@@ -179,5 +179,32 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Register dependency fence: the compiler must assume `r` changes here. Placed
+// after tcgen05.wait::ld it keeps every read of a tcgen05.ld destination after
+// the wait; placed after tcgen05.wait::st it keeps the source registers of a
+// tcgen05.st from being reused before the store has read them.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
+// Load 32 columns and wait: the registers are valid on return.
+__device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]) {
+  tmem_ld32(taddr, r);
+  tmem_wait_ld();
+  reg_fence(r);
+}
+
+// Store 32 columns and wait until the store has read the registers.
+__device__ __forceinline__ void tmem_st32_wait(uint32_t taddr, uint32_t (&r)[32]) {
+  tmem_st32(taddr, r);
+  tmem_wait_st();
+  reg_fence(r);
+}
+
 }  // namespace sm100
 }  // namespace pkv

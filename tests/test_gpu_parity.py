@@ -112,6 +112,8 @@ RAGGED = [
     (6, 8, 4, 1, 64, 16, "f16", (1, 17), 300),
     (7, 2, 32, 2, 64, 256, "bf16", (130, 1), 700),
     (8, 7, 16, 16, 64, 16, "f32", (1,), 300),
+    (9, 3, 8, 8, 128, 256, "bf16", (130, 1), 400),      # g = 1: single-query-tile prefill kernel
+    (10, 4, 16, 4, 64, 32, "f16", (200, 1, 70), 600),   # page 32 < tile: several pages per TMA tile
 ]
 
 
