@@ -8,18 +8,22 @@
 // of the same GQA group): both query tiles read the same K/V tiles and have the
 // same causal mask, so every K/V tile fetched by TMA feeds four MMAs.
 //
-//   warp 0      TMA producer: Q of both heads, then K_j, V_j into a 3-slot ring
+//   warp 0      TMA producer: Q of both heads, then K_j, V_j into a ring of
+//               5 (head_dim 128) or 8 (head_dim 64) shared-memory slots
 //               (V rows past kv_len zeroed in the last tile)
-//   warp 1      TMEM owner (512 columns) and MMA issuer:
-//               S_w = Q_w K_j^T  (w = 0, 1; TMEM columns 128 w),
-//               O_w += P_w V_{j-1} (TMEM columns 256 + 128 w)
+//   warp 1      TMEM owner (512 columns) and MMA issuer, per KV tile j and
+//               query tile w: O_w += P_w V_{j-1} (A operand read from TMEM),
+//               then S_w = Q_w K_j^T into the same TMEM columns; the MMA pipe
+//               runs in issue order, so S_w is only overwritten after the PV
+//               that reads P_w, and S_w complete implies that PV complete
 //   warps 2-5   softmax of query tile 0, one thread per row
 //   warps 6-9   softmax of query tile 1
-// The softmax copies its S row to registers and frees the S buffer at once, so
-// the next QK^T into it can start; a masked max pass (only for tiles on the
-// causal diagonal) and one exp pass (scale folded into an FFMA, raw ex2) write
-// P in bf16/fp16 to shared memory (128-byte swizzled K-major, PV's A operand).
-// O is rescaled in TMEM only when a row's max grows by more than 2^8.
+// The softmax reads its S row from TMEM, takes the row max (causal mask only on
+// tiles that cross the diagonal), and writes P = exp2(scale * S - m) in
+// bf16/fp16 back over S with tcgen05.st (packed pairs: the TMEM layout of a
+// 16-bit A operand). O is rescaled in TMEM only when a row's max grows by more
+// than 2^8. P never goes through shared memory, which leaves room for a deep
+// K/V ring.
 // Every mbarrier wait is bounded (PKV_DEV_TIMEOUT); TMEM accesses are
 // warp-uniform.
 #include <cuda.h>
@@ -64,13 +68,23 @@ struct Tile2 {
 template <int D>
 struct Cfg2 {
   static constexpr int HALVES = D / 64;
-  static constexpr int NSLOT = D == 128 ? 3 : 4;
+  static constexpr int NSLOT = D == 128 ? 5 : 8;
   static constexpr uint32_t Q_BYTES = BM * D * 2;       // one query tile
   static constexpr uint32_t SLOT_BYTES = BN * D * 2;
-  static constexpr uint32_t P_BYTES = BM * BN * 2;      // one P tile
-  static constexpr uint32_t SMEM = NWG * Q_BYTES + NSLOT * SLOT_BYTES + NWG * P_BYTES + 1024;
+  static constexpr uint32_t SMEM = NWG * Q_BYTES + NSLOT * SLOT_BYTES + 1024;
   static_assert(SMEM <= 232448, "shared memory");
 };
+
+// tcgen05.mma .kind::f16 with the A operand (M x K, 16-bit, packed in pairs per
+// 32-bit column, one row per lane) in TMEM and B in shared memory.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 __device__ __forceinline__ bool wait2(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* ctrl,
                                       int32_t* dev_status) {
@@ -118,10 +132,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   unsigned char* sQ = sm;                                   // [NWG][Q tile]
   unsigned char* sRing = sQ + NWG * C::Q_BYTES;             // [NS][slot]
-  unsigned char* sP = sRing + NS * C::SLOT_BYTES;           // [NWG][P tile]
 
-  __shared__ __align__(8) uint64_t bar_q, bar_full[NS], bar_empty[NS], bar_sfull[NWG], bar_sfree[NWG],
-      bar_pfull[NWG], bar_odone[NWG], bar_vfix, bar_drain;
+  __shared__ __align__(8) uint64_t bar_q, bar_full[NS], bar_empty[NS], bar_sfull[NWG], bar_pfull[NWG],
+      bar_odone[NWG], bar_vfix, bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ Tile2 s_tile;
   __shared__ volatile int s_abort;
@@ -136,7 +149,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int w = 0; w < NWG; ++w) {
       mbar_init(&bar_sfull[w], 1);
-      mbar_init(&bar_sfree[w], 128);
       mbar_init(&bar_pfull[w], 128);
       mbar_init(&bar_odone[w], 1);
     }
@@ -158,9 +170,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int g = p.Hq / p.Hkv;
 
   uint32_t ring = 0;                   // producer / MMA
-  uint32_t s_use[NWG] = {0, 0};        // MMA: QK issued per S buffer
   uint32_t p_use[NWG] = {0, 0};        // MMA: P consumed per group
-  uint32_t my_s = 0, my_o = 0;         // softmax thread: S waits, PV waits of its group
+  uint32_t my_s = 0;                   // softmax thread: S waits of its group
   uint32_t tile_cnt = 0;
   uint32_t fills[NS];
 #pragma unroll
@@ -288,9 +299,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t base = ring;
         bool ok = wait2(&bar_q, tile_cnt & 1, &s_abort, p.ctrl, p.dev_status);
         tc_fence_after();
-        // per KV tile j, for each query tile w: S_w = Q_w K_j^T, then O_w += P_w V_{j-1}
-        // (both wait for the end of w's softmax of tile j-1, so the other query
-        // tile's MMAs keep the tensor core busy meanwhile)
+        // per KV tile j and query tile w: O_w += P_w V_{j-1}, then S_w = Q_w K_j^T
         for (int j = 0; j <= ti.n_kv && ok; ++j) {
           const bool qk = j < ti.n_kv, pv = j > 0;
           const uint32_t ik = base + 2 * j, iv = base + 2 * j - 1;
@@ -310,13 +319,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const uint32_t v_base = smem_u32(sRing + vslot * C::SLOT_BYTES);
 #pragma unroll
           for (int w = 0; w < NWG; ++w) {
-            if (qk) {
-              if (!wait2(&bar_sfree[w], (s_use[w] & 1) ^ 1, &s_abort, p.ctrl, p.dev_status)) {
+            if (pv) {
+              if (!wait2(&bar_pfull[w], p_use[w] & 1, &s_abort, p.ctrl, p.dev_status)) {
                 ok = false;
                 break;
               }
-              ++s_use[w];
+              ++p_use[w];
               tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < BN / 16; ++kk) {
+                const uint64_t bd = smem_desc(v_base + kk * 16 * 128, BN * 128, 1024, LAYOUT_SW128);
+                mma_f16_ts(tmem + 256 + w * 128, tmem + w * 128 + kk * 8, bd, id_pv, (j > 1 || kk > 0) ? 1u : 0u);
+              }
+              if (j == ti.n_kv) mma_commit(&bar_odone[w]);
+            }
+            if (qk) {
               const uint32_t q_base = smem_u32(sQ + w * C::Q_BYTES);
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
@@ -326,22 +343,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                            smem_desc(k_base + offk, 16, 1024, LAYOUT_SW128), id_qk, kk > 0 ? 1u : 0u);
               }
               mma_commit(&bar_sfull[w]);
-            }
-            if (pv) {
-              if (!wait2(&bar_pfull[w], p_use[w] & 1, &s_abort, p.ctrl, p.dev_status)) {
-                ok = false;
-                break;
-              }
-              ++p_use[w];
-              tc_fence_after();
-              const uint32_t p_base = smem_u32(sP + w * C::P_BYTES);
-#pragma unroll
-              for (int kk = 0; kk < BN / 16; ++kk) {
-                const uint64_t ad = smem_desc(p_base + (kk / 4) * BM * 128 + (kk % 4) * 32, 16, 1024, LAYOUT_SW128);
-                const uint64_t bd = smem_desc(v_base + kk * 16 * 128, BN * 128, 1024, LAYOUT_SW128);
-                mma_f16_ss(tmem + 256 + w * 128, ad, bd, id_pv, (j > 1 || kk > 0) ? 1u : 0u);
-              }
-              mma_commit(&bar_odone[w]);
             }
           }
           if (!ok) break;
@@ -359,10 +360,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint32_t s_col = w * 128, o_col = 256 + w * 128;
       const int p_i = min(ti.p_first + i, ti.L - 1);
       const float sc = p.scale_log2;
-      unsigned char* prow = sP + w * C::P_BYTES + i * 128;
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
       for (int j = 0; j < ti.n_kv && ok; ++j) {
+        // S_w complete also means every earlier MMA (the PV that read P_w) is done
         if (!__all_sync(0xffffffffu, wait2(&bar_sfull[w], my_s & 1, &s_abort, p.ctrl, p.dev_status))) {
           ok = false;
           break;
@@ -371,92 +372,75 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_after();
         const bool masked = j >= ti.j_mask;
         const int lim = p_i - j * BN;               // keys with index <= lim are visible
-        // pass 1: row max of the raw scores (scale > 0 keeps the order)
+        uint32_t r[BN / 32][32];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) tmem_ld32(tmem + lrow + s_col + c * 32, r[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) reg_fence(r[c]);
+        // row max of the raw scores (scale > 0 keeps the order)
         float mx[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+        if (masked) {
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32_wait(tmem + lrow + s_col + c * 32, r);
-          if (masked) {
+          for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              mx[e & 7] = fmaxf(mx[e & 7], c * 32 + e <= lim ? __uint_as_float(r[e]) : -INFINITY);
-          } else {
+            for (int e = 0; e < 32; ++e) {
+              if (c * 32 + e > lim) r[c][e] = __float_as_uint(-INFINITY);
+              mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(r[c][e]));
+            }
+        } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(r[e]));
-          }
+          for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(r[c][e]));
         }
         const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sc;
         const bool first = j == 0;
         const bool grow = first || mt > m_run + RESCALE_LOG2;
         const float m_new = grow ? fmaxf(mt, m_run) : m_run;
-        if (!first) {
-          // PV_{j-1} must be done before P is overwritten or O rescaled
-          if (!__all_sync(0xffffffffu, wait2(&bar_odone[w], my_o & 1, &s_abort, p.ctrl, p.dev_status))) {
-            ok = false;
-            break;
-          }
-          ++my_o;
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, grow)) {
-            const float alpha = grow ? ex2(m_run - m_new) : 1.f;
-            l_run *= alpha;
+        if (!first && __any_sync(0xffffffffu, grow)) {
+          const float alpha = grow ? ex2(m_run - m_new) : 1.f;
+          l_run *= alpha;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t r[32];
-              tmem_ld32_wait(tmem + lrow + o_col + c * 32, r);
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32_wait(tmem + lrow + o_col + c * 32, o);
 #pragma unroll
-              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-              tmem_st32_wait(tmem + lrow + o_col + c * 32, r);
-            }
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32_wait(tmem + lrow + o_col + c * 32, o);
           }
         }
         m_run = m_new;
-        // pass 2: P = exp2(scale * S - m) in 16-bit into shared memory, row sum in fp32
+        // P = exp2(scale * S - m) in 16-bit, packed pairs over the first 64 S
+        // columns (masked keys hold -inf: exp2 gives 0 since scale > 0)
         const float neg_m = -m_run;
         float ls[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) ls[k] = 0.f;
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32_wait(tmem + lrow + s_col + c * 32, r);
-          if (c == BN / 32 - 1) {
-            tc_fence_before();
-            mbar_arrive(&bar_sfree[w]);             // S fully read: the next Q K^T may overwrite it
-          }
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pw[32];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {          // 4 x 8 keys = one 16-byte chunk of P each
-            uint32_t wv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int k0 = q4 * 8 + 2 * e;
-              float a = ex2(fmaf(__uint_as_float(r[k0]), sc, neg_m));
-              float b = ex2(fmaf(__uint_as_float(r[k0 + 1]), sc, neg_m));
-              if (masked) {
-                a = c * 32 + k0 <= lim ? a : 0.f;
-                b = c * 32 + k0 + 1 <= lim ? b : 0.f;
-              }
-              ls[(2 * e) & 7] += a;
-              ls[(2 * e + 1) & 7] += b;
-              wv[e] = pack_h2<T>(a, b);
-            }
-            const int ch = c * 4 + q4;              // 16-byte chunk index along the 128 keys
-            const int hf = ch >> 3, c8 = ch & 7;
-            *reinterpret_cast<uint4*>(prow + hf * BM * 128 + ((c8 ^ (i & 7)) << 4)) =
-                make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          for (int e = 0; e < 32; ++e) {
+            const int k0 = hf * 64 + 2 * e;
+            const float a = ex2(fmaf(__uint_as_float(r[k0 >> 5][k0 & 31]), sc, neg_m));
+            const float b = ex2(fmaf(__uint_as_float(r[(k0 + 1) >> 5][(k0 + 1) & 31]), sc, neg_m));
+            ls[(2 * e) & 7] += a;
+            ls[(2 * e + 1) & 7] += b;
+            pw[e] = pack_h2<T>(a, b);
           }
+          tmem_st32(tmem + lrow + s_col + hf * 32, pw);
+          tmem_wait_st();
+          reg_fence(pw);
         }
         l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&bar_pfull[w]);
       }
-      if (ok) ok = __all_sync(0xffffffffu, wait2(&bar_odone[w], my_o & 1, &s_abort, p.ctrl, p.dev_status));
-      ++my_o;
+      if (ok) ok = __all_sync(0xffffffffu, wait2(&bar_odone[w], tile_cnt & 1, &s_abort, p.ctrl, p.dev_status));
       if (ok) ok = __all_sync(0xffffffffu, wait2(&bar_vfix, tile_cnt & 1, &s_abort, p.ctrl, p.dev_status));
       tc_fence_after();
       if (ok) {
@@ -465,16 +449,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         T* dst = (T*)p.out + ((int64_t)(ti.row0 + i) * p.Hq + ti.h + w) * D;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32_wait(tmem + lrow + o_col + c * 32, r);
+          uint32_t o[32];
+          tmem_ld32_wait(tmem + lrow + o_col + c * 32, o);
           if (!store) continue;
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint4 pk;
-            pk.x = pack_h2<T>(__uint_as_float(r[v * 8 + 0]) * inv, __uint_as_float(r[v * 8 + 1]) * inv);
-            pk.y = pack_h2<T>(__uint_as_float(r[v * 8 + 2]) * inv, __uint_as_float(r[v * 8 + 3]) * inv);
-            pk.z = pack_h2<T>(__uint_as_float(r[v * 8 + 4]) * inv, __uint_as_float(r[v * 8 + 5]) * inv);
-            pk.w = pack_h2<T>(__uint_as_float(r[v * 8 + 6]) * inv, __uint_as_float(r[v * 8 + 7]) * inv);
+            pk.x = pack_h2<T>(__uint_as_float(o[v * 8 + 0]) * inv, __uint_as_float(o[v * 8 + 1]) * inv);
+            pk.y = pack_h2<T>(__uint_as_float(o[v * 8 + 2]) * inv, __uint_as_float(o[v * 8 + 3]) * inv);
+            pk.z = pack_h2<T>(__uint_as_float(o[v * 8 + 4]) * inv, __uint_as_float(o[v * 8 + 5]) * inv);
+            pk.w = pack_h2<T>(__uint_as_float(o[v * 8 + 6]) * inv, __uint_as_float(o[v * 8 + 7]) * inv);
             *reinterpret_cast<uint4*>(dst + c * 32 + v * 8) = pk;
           }
         }
