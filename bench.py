@@ -9,7 +9,9 @@ paged_attention (work plan, prefill-chunk kernel, decode rows, split combine).
 
 Prints one JSON line. `value` is tokens/s (packed rows per second, whole job),
 timed with CUDA events per step on the launching stream, with the L2 flushed
-(a 512 MB write) between steps outside the timed events. `e2e` is the same
+(a 512 MB write) between steps outside the timed events. The step is captured
+once in a CUDA graph and replayed (the library plans on the device, so replays
+need no host work); `eager` reports the same step launched call by call. `e2e` is the same
 metric through the public calls with host buffers: per step the host packs the
 tick, copies its inputs from pinned memory, runs the calls, and reads the
 outputs back. `--impl reference` times the CPU oracle on a bounded sample of the
@@ -344,12 +346,38 @@ def main():
         b.record(stream)
     torch.cuda.synchronize()
     barrier()
-    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    eager_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+
+    # pass G: the same step captured once in a CUDA graph and replayed (the work
+    # plan is computed on the device, so a replay needs no host work at all)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            step()
+    stream.wait_stream(cap)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        flush.zero_()
+        graph.replay()
+    evg = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for a, b in evg:
+        flush.zero_()
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    assert binding.device_status() == 0
+    ms = sum(a.elapsed_time(b) for a, b in evg) / args.steps
     if world > 1:
         import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
+        t = torch.tensor([ms, eager_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms, eager_ms = float(t[0].item()), float(t[1].item())
     value = world * T / (ms / 1000.0)
 
     # pass B: per-kernel device time (events on the launch stream around each kernel)
@@ -438,12 +466,15 @@ def main():
         "vs_baseline": None, "dtype": s.dtype, "data": "synthetic",
         "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
                    "tokens_per_step": T, "l2": "flushed between steps (512 MB write, outside the step events)",
+                   "launch": "CUDA graph replay of the step (eager launches reported under eager)",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "roofline": roof,
         "roofline_decode": roof_decode,
         "decode_hbm_gbs": decode_gbs,
         "kernels": per_kernel,
         "cpu_baseline": cpu,
+        "eager": {"value": world * T / (eager_ms / 1000.0), "ms_per_step": eager_ms,
+                  "note": "same step launched call by call instead of replayed from the captured graph"},
         "e2e": {"value": world * T / (e2e_avg / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_avg},
         "gpu_launches": int(round(launches_per_step * args.steps)),

@@ -43,11 +43,12 @@ PlanLayout plan_layout(int32_t B, int32_t T, int32_t Hq, int32_t Hkv, int32_t D,
   return L;
 }
 
+// binary search over a copy in shared memory (or the input itself when it is too big)
 __device__ __forceinline__ int upper_bound_i32(const int32_t* a, int n, int x) {
   int lo = 0, hi = n;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if (__ldg(a + mid) <= x) lo = mid + 1; else hi = mid;
+    if (a[mid] <= x) lo = mid + 1; else hi = mid;
   }
   return lo;
 }
@@ -90,6 +91,44 @@ __device__ int block_scan_excl(int v, int* total, int* sm) {
   return res;
 }
 
+// Exclusive scan of three values at once over the 1024 threads of the block.
+__device__ void block_scan3(const int (&v)[3], int (&ex)[3], int (&tot)[3], int (*sm)[32]) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x[3] = {v[0], v[1], v[2]};
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const int y = __shfl_up_sync(0xffffffffu, x[k], o);
+      if (lane >= o) x[k] += y;
+    }
+  }
+  if (lane == 31) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) sm[k][w] = x[k];
+  }
+  __syncthreads();
+  if (w == 0) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      int s = sm[k][lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += y;
+      }
+      sm[k][lane] = s;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    ex[k] = (w > 0 ? sm[k][w - 1] : 0) + x[k] - v[k];
+    tot[k] = sm[k][31];
+  }
+  __syncthreads();
+}
+
 constexpr int HIST = 2048;
 
 struct SeqInfo {
@@ -99,60 +138,69 @@ struct SeqInfo {
 
 __device__ __forceinline__ SeqInfo seq_info(const PlanArgs& a, int b) {
   SeqInfo s;
-  const int c0 = __ldg(a.cu + b), c1 = __ldg(a.cu + b + 1);
+  const int c0 = a.cu[b], c1 = a.cu[b + 1];
   s.q = c1 - c0;
-  s.L = __ldg(a.kv_lens + b);
+  s.L = a.kv_lens[b];
   s.bad = s.q < 0 || c0 < 0 || c1 > a.T ||
           (s.q > 0 && (s.L < s.q || s.L > a.max_kv_len || s.L > a.table_cap));
   s.tc = !s.bad && a.tc_min_q > 0 && s.q >= a.tc_min_q;
   return s;
 }
 
-// splits of row r for split size C (0 when the row has no row-path work)
-__device__ __forceinline__ int row_splits(const PlanArgs& a, int r, int C, int* seq_out) {
-  const int b = upper_bound_i32(a.cu, a.B + 1, r) - 1;
-  *seq_out = -1;
-  if (b < 0 || b >= a.B) return 0;
-  const SeqInfo s = seq_info(a, b);
-  const int c0 = __ldg(a.cu + b);
-  if (s.bad || s.tc || r < c0 || r >= c0 + s.q) return 0;
-  *seq_out = b;
-  const int limit = s.L - s.q + (r - c0) + 1;
-  return (limit + C - 1) / C;
-}
+constexpr int PLAN_SMEM_SEQS = 12000;   // sequences whose lengths are staged in shared memory
 
-__global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a, int32_t* dev_status) {
+__global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_status) {
+  // stage cu_seqlens_q and kv_lens in shared memory: every row below searches them
+  extern __shared__ int32_t s_seq[];
+  PlanArgs a = a_in;
+  if (a_in.B <= PLAN_SMEM_SEQS) {
+    for (int i = threadIdx.x; i <= a_in.B; i += blockDim.x) s_seq[i] = __ldg(a_in.cu + i);
+    for (int i = threadIdx.x; i < a_in.B; i += blockDim.x) s_seq[a_in.B + 1 + i] = __ldg(a_in.kv_lens + i);
+    a.cu = s_seq;
+    a.kv_lens = s_seq + a_in.B + 1;
+    __syncthreads();
+  }
   int32_t* ctrl = (int32_t*)(a.ws + a.lay.ctrl);
   int32_t* row_seq = (int32_t*)(a.ws + a.lay.row_seq);
   int32_t* item_begin = (int32_t*)(a.ws + a.lay.row_item_begin);
   int32_t* part_begin = (int32_t*)(a.ws + a.lay.row_part_begin);
   int32_t* split_rows = (int32_t*)(a.ws + a.lay.split_rows);
-  int32_t* pair_begin = (int32_t*)(a.ws + a.lay.seq_pair_begin);
+  int32_t* pair_begin_g = (int32_t*)(a.ws + a.lay.seq_pair_begin);
+  int32_t* pair_begin = a_in.B <= PLAN_SMEM_SEQS ? s_seq + 2 * a_in.B + 1 : pair_begin_g;
   int2* pairs = (int2*)(a.ws + a.lay.tc_pairs);
 
   __shared__ unsigned long long s_keys;
-  __shared__ int s_err, s_cnt;
+  __shared__ int s_err;
   __shared__ int sm[32];
+  __shared__ int sm3[3][32];
   __shared__ int hist[HIST];
   const int tid = threadIdx.x;
   if (tid == 0) {
     s_keys = 0;
     s_err = 0;
-    s_cnt = 0;
-    if (__ldg(a.cu) != 0 || __ldg(a.cu + a.B) != a.T) s_err = PKV_DEV_BAD_LENGTHS;
+    if (a.cu[0] != 0 || a.cu[a.B] != a.T) s_err = PKV_DEV_BAD_LENGTHS;
   }
   __syncthreads();
 
   // pass 1: check every sequence; count the keys the row path will visit
   unsigned long long my_keys = 0;
+  int my_err = 0;
   for (int b = tid; b < a.B; b += blockDim.x) {
     const SeqInfo s = seq_info(a, b);
-    if (s.bad) atomicOr(&s_err, PKV_DEV_BAD_LENGTHS);
+    if (s.bad) my_err = PKV_DEV_BAD_LENGTHS;
     if (!s.bad && !s.tc && s.q > 0)
       my_keys += (unsigned long long)s.q * (unsigned long long)(s.L - s.q) +
                  (unsigned long long)s.q * (s.q + 1) / 2;
   }
-  atomicAdd(&s_keys, my_keys);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    my_keys += __shfl_xor_sync(0xffffffffu, my_keys, o);
+    my_err |= __shfl_xor_sync(0xffffffffu, my_err, o);
+  }
+  if ((tid & 31) == 0) {
+    atomicAdd(&s_keys, my_keys);
+    if (my_err) atomicOr(&s_err, my_err);
+  }
   __syncthreads();
 
   // split size: about target_items items, at least chunk_min keys, multiple of 64
@@ -163,44 +211,54 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a, int32_t* dev_sta
   const long long c_max = ((long long)a.max_kv_len + 63) / 64 * 64;
   if (C > c_max) C = c_max < 64 ? 64 : c_max;
 
-  // grow C until the partial results fit the workspace
+  // Each thread owns a contiguous run of rows and walks the sequence
+  // boundaries along it; one 3-value block scan turns the per-thread counts
+  // (items, partial slots, split rows) into offsets.
+  const int R = (a.T + blockDim.x - 1) / blockDim.x;
+  const int r_begin = min(a.T, tid * R), r_end = min(a.T, r_begin + R);
+  auto for_rows = [&](auto&& f) {
+    if (r_begin >= r_end) return;
+    int b = upper_bound_i32(a.cu, a.B + 1, r_begin) - 1;
+    for (int r = r_begin; r < r_end; ++r) {
+      while (b + 1 < a.B && a.cu[b + 1] <= r) ++b;
+      int n = 0, bb = -1;
+      if (b >= 0 && b < a.B) {
+        const SeqInfo si = seq_info(a, b);
+        const int c0 = a.cu[b];
+        if (!si.bad && !si.tc && r >= c0 && r < c0 + si.q) {
+          bb = b;
+          n = (int)((si.L - si.q + (r - c0) + 1 + C - 1) / C);
+        }
+      }
+      f(r, n, bb);
+    }
+  };
+  int ex[3], tot[3];
   for (int guard = 0; guard < 40; ++guard) {
-    int parts = 0;
-    for (int r = tid; r < a.T; r += blockDim.x) {
-      int b;
-      const int n = row_splits(a, r, (int)C, &b);
-      if (n > 1) parts += n * a.Hkv;
-    }
-    atomicAdd(&s_cnt, parts);
-    __syncthreads();
-    const int total = s_cnt;
-    __syncthreads();
-    if (tid == 0) s_cnt = 0;
-    __syncthreads();
-    if (total <= a.lay.partial_cap || C >= c_max) break;
-    C = C * 2 < c_max ? C * 2 : c_max;
+    int cnt[3] = {0, 0, 0};
+    for_rows([&](int, int n, int) {
+      cnt[0] += n * a.Hkv;
+      if (n > 1) {
+        cnt[1] += n * a.Hkv;
+        cnt[2] += 1;
+      }
+    });
+    block_scan3(cnt, ex, tot, sm3);
+    if (tot[1] <= a.lay.partial_cap || C >= c_max) break;
+    C = C * 2 < c_max ? C * 2 : c_max;   // grow the split until the partials fit
   }
-
-  // pass 2: per-row item and partial ranges, and the list of split rows
-  int carry_items = 0, carry_parts = 0, carry_split = 0;
-  for (int base = 0; base < a.T; base += blockDim.x) {
-    const int r = base + tid;
-    int n = 0, b = -1;
-    if (r < a.T) n = row_splits(a, r, (int)C, &b);
-    int t_items, t_parts, t_split;
-    const int e_items = block_scan_excl(n * a.Hkv, &t_items, sm);
-    const int e_parts = block_scan_excl(n > 1 ? n * a.Hkv : 0, &t_parts, sm);
-    const int e_split = block_scan_excl(n > 1 ? 1 : 0, &t_split, sm);
-    if (r < a.T) {
-      row_seq[r] = b;
-      item_begin[r] = carry_items + e_items;
-      part_begin[r] = n > 1 ? carry_parts + e_parts : -1;
-      if (n > 1) split_rows[carry_split + e_split] = r;
-    }
-    carry_items += t_items;
-    carry_parts += t_parts;
-    carry_split += t_split;
+  {
+    int it = ex[0], pt = ex[1], sp = ex[2];
+    for_rows([&](int r, int n, int bb) {
+      row_seq[r] = bb;
+      item_begin[r] = it;
+      part_begin[r] = n > 1 ? pt : -1;
+      if (n > 1) split_rows[sp++] = r;
+      it += n * a.Hkv;
+      if (n > 1) pt += n * a.Hkv;
+    });
   }
+  const int carry_items = tot[0], carry_parts = tot[1], carry_split = tot[2];
   if (tid == 0) item_begin[a.T] = carry_items;
 
   // pass 3: (sequence, q tile) pairs of the prefill kernel, longest first
@@ -218,11 +276,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a, int32_t* dev_sta
     carry_pairs += t;
   }
   if (tid == 0) pair_begin[a.B] = carry_pairs;
+  __syncthreads();
   const int n_pairs = carry_pairs;
   for (int i = tid; i < HIST; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   auto pair_work = [&](int p, int* b_out, int* qt_out) {
-    const int b = upper_bound_written(pair_begin, a.B + 1, p) - 1;
+    const int b = upper_bound_written(pair_begin, a.B + 1, p) - 1;   // shared memory when B fits
     const int qt = p - pair_begin[b];
     const SeqInfo s = seq_info(a, b);
     const int q1 = min(s.q, (qt + 1) * TC_BM);
@@ -277,8 +336,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a, int32_t* dev_sta
 }
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
+  static cudaError_t attr = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (3 * PLAN_SMEM_SEQS + 2) * 4);
+  if (attr != cudaSuccess) return attr;
+  const size_t smem = a.B <= PLAN_SMEM_SEQS ? (size_t)(3 * a.B + 2) * 4 : 0;
   KernelTimer timer("plan", s);
-  plan_kernel<<<1, 1024, 0, s>>>(a, a.dev_status);
+  plan_kernel<<<1, 1024, smem, s>>>(a, a.dev_status);
   return cudaGetLastError();
 }
 
