@@ -235,14 +235,12 @@ def oracle_sample(w, seconds=12.0, seed=0):
 # ---------------------------------------------------------------------------
 
 def dist_setup(n_gpus):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from paged_kv_attention_mapping_gb300 import dist as D
+    rank, local, world = D.rank_world()
     if world > 1:
-        import torch.distributed as dist
         import torch
         torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        D.init("nccl")
     return world, rank, local
 
 
@@ -329,10 +327,8 @@ def main():
     torch.cuda.synchronize()
     assert binding.device_status() == 0
 
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
+    from paged_kv_attention_mapping_gb300 import dist as D
+    barrier = D.barrier
 
     # pass A: the headline number (no per-kernel events)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -373,12 +369,8 @@ def main():
     barrier()
     assert binding.device_status() == 0
     ms = sum(a.elapsed_time(b) for a, b in evg) / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, eager_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, eager_ms = float(t[0].item()), float(t[1].item())
-    value = world * T / (ms / 1000.0)
+    ms, eager_ms = D.max_over_ranks([ms, eager_ms], device=dev)
+    value = D.aggregate_tokens_per_s(T, ms, world)
 
     # pass B: per-kernel device time (events on the launch stream around each kernel)
     binding.set_kernel_timing(True)
@@ -425,12 +417,7 @@ def main():
         t0 = time.perf_counter()
         e2e_step()
         e2e_ms.append((time.perf_counter() - t0) * 1000.0)
-    e2e_avg = statistics.mean(e2e_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_avg], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_avg = float(t.item())
+    e2e_avg = D.max_over_ranks([statistics.mean(e2e_ms)], device=dev)[0]
     clk.__exit__(None, None, None)
     h2d = meta_bytes + sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v))
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
