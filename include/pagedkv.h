@@ -191,6 +191,52 @@ int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, const int32_
                         void* workspace, size_t workspace_bytes, pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Host page pool and prefix cache (no device work; host memory only).
+ *
+ * A fixed pool of page ids with per-page reference counts, and a cache of
+ * complete prompt blocks keyed by a hash chained over the blocks before them
+ * (Helios README, "Paged attention": pages come from a free list and return
+ * to the pool when the last request or prefix-cache entry holding them lets
+ * go; Helios blog, "Prefix caching": complete page-size prompt blocks are
+ * hashed with the previous block's hash, a request reuses the longest matching
+ * chain's pages, partial blocks are not stored, entries have a sliding TTL and
+ * eviction takes unused leaf blocks first).
+ *  - pkv_pool_alloc hands out the lowest free ids first, each with count 1;
+ *    PKV_E_CAPACITY (nothing taken) when fewer than n pages are free.
+ *  - pkv_pool_retain / pkv_pool_release add / drop one reference per listed
+ *    page (a page may be listed several times); a page whose count reaches 0
+ *    is free again. PKV_E_PAGES (nothing changed) for an id outside the pool,
+ *    a free page, or more releases than references.
+ *  - pkv_prefix_lookup walks tokens[0 .. n_tokens) block by block (page_size
+ *    tokens each) and returns the number of leading blocks found in the cache
+ *    (at most max_pages); their page ids go to pages[] and each gets one more
+ *    reference, now owned by the caller; their last-use time becomes `now`.
+ *  - pkv_prefix_insert stores every complete block of tokens not yet cached,
+ *    on the caller's page for that block (pages[b] for block b); the cache
+ *    takes one reference per stored page. Returns the number of new entries.
+ *  - pkv_prefix_evict drops unused leaf entries (the cache holds the only
+ *    reference and no cached block continues them): first every entry unused
+ *    for more than `ttl` (sliding), then, oldest last use first, until at
+ *    least want_free pages are free or nothing is evictable. Returns the
+ *    number of entries dropped.
+ * The pool object is not thread-safe; callers serialise access.
+ */
+typedef struct pkv_pool pkv_pool;
+int pkv_pool_create(int32_t num_pages, int32_t page_size, pkv_pool** out);
+void pkv_pool_destroy(pkv_pool* pool);
+int pkv_pool_alloc(pkv_pool* pool, int32_t n, int32_t* pages);
+int pkv_pool_retain(pkv_pool* pool, const int32_t* pages, int32_t n);
+int pkv_pool_release(pkv_pool* pool, const int32_t* pages, int32_t n);
+int pkv_pool_free_count(const pkv_pool* pool);
+int pkv_pool_refcount(const pkv_pool* pool, int32_t page);
+int pkv_prefix_lookup(pkv_pool* pool, const int32_t* tokens, int32_t n_tokens, double now, int32_t* pages,
+                      int32_t max_pages);
+int pkv_prefix_insert(pkv_pool* pool, const int32_t* tokens, int32_t n_tokens, const int32_t* pages,
+                      int32_t n_pages, double now);
+int pkv_prefix_evict(pkv_pool* pool, double now, double ttl, int32_t want_free);
+int pkv_prefix_size(const pkv_pool* pool);
+
+/* ---------------------------------------------------------------------------
  * pkv_paged_attention_no_alloc — pkv_paged_attention without a workspace
  * argument, for callers that cannot allocate device memory (for example code
  * running inside a memory pool's or custom allocator's own callbacks, or a

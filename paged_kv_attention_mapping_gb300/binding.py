@@ -31,6 +31,17 @@ EXPORTED = (
     "pkv_kernel_times",
     "pkv_version",
     "pkv_last_error",
+    "pkv_pool_create",
+    "pkv_pool_destroy",
+    "pkv_pool_alloc",
+    "pkv_pool_retain",
+    "pkv_pool_release",
+    "pkv_pool_free_count",
+    "pkv_pool_refcount",
+    "pkv_prefix_lookup",
+    "pkv_prefix_insert",
+    "pkv_prefix_evict",
+    "pkv_prefix_size",
 )
 
 
@@ -82,6 +93,25 @@ def lib():
     L.pkv_kernel_times.restype = ctypes.c_int
     L.pkv_last_error.argtypes = []
     L.pkv_last_error.restype = ctypes.c_char_p
+    L.pkv_pool_create.argtypes = [i32, i32, ctypes.POINTER(vp)]
+    L.pkv_pool_create.restype = ctypes.c_int
+    L.pkv_pool_destroy.argtypes = [vp]
+    L.pkv_pool_destroy.restype = None
+    for name in ("pkv_pool_alloc", "pkv_pool_retain", "pkv_pool_release"):
+        getattr(L, name).argtypes = [vp, P32, i32] if name != "pkv_pool_alloc" else [vp, i32, P32]
+        getattr(L, name).restype = ctypes.c_int
+    L.pkv_pool_free_count.argtypes = [vp]
+    L.pkv_pool_free_count.restype = ctypes.c_int
+    L.pkv_pool_refcount.argtypes = [vp, i32]
+    L.pkv_pool_refcount.restype = ctypes.c_int
+    L.pkv_prefix_lookup.argtypes = [vp, P32, i32, ctypes.c_double, P32, i32]
+    L.pkv_prefix_lookup.restype = ctypes.c_int
+    L.pkv_prefix_insert.argtypes = [vp, P32, i32, P32, i32, ctypes.c_double]
+    L.pkv_prefix_insert.restype = ctypes.c_int
+    L.pkv_prefix_evict.argtypes = [vp, ctypes.c_double, ctypes.c_double, i32]
+    L.pkv_prefix_evict.restype = ctypes.c_int
+    L.pkv_prefix_size.argtypes = [vp]
+    L.pkv_prefix_size.restype = ctypes.c_int
     L.pkv_version.argtypes = []
     L.pkv_version.restype = ctypes.c_char_p
     _lib = L
@@ -268,3 +298,80 @@ def kernel_times(max_kernels: int = 32):
     if n < 0:
         raise PagedKVError(n, "pkv_kernel_times")
     return {names[i].decode(): (int(launches[i]), float(total[i])) for i in range(n)}
+
+
+# ---------------------------------------------------------------------------
+# host page pool and prefix cache
+
+class PagePool:
+    """The library's host page pool (pkv_pool_*, pkv_prefix_*)."""
+
+    def __init__(self, num_pages: int, page_size: int):
+        self._h = ctypes.c_void_p()
+        _check(lib().pkv_pool_create(int(num_pages), int(page_size), ctypes.byref(self._h)), "pkv_pool_create")
+        self.num_pages, self.page_size = int(num_pages), int(page_size)
+
+    def close(self):
+        if self._h:
+            lib().pkv_pool_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _arr(xs):
+        a = np.ascontiguousarray(np.asarray(xs, dtype=np.int32))
+        return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+    def alloc(self, n: int):
+        a = np.zeros(max(n, 1), dtype=np.int32)
+        _check(lib().pkv_pool_alloc(self._h, int(n), a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))), "pkv_pool_alloc")
+        return [int(x) for x in a[:n]]
+
+    def retain(self, pages):
+        a, p = self._arr(pages)
+        _check(lib().pkv_pool_retain(self._h, p, len(a)), "pkv_pool_retain")
+
+    def release(self, pages):
+        a, p = self._arr(pages)
+        _check(lib().pkv_pool_release(self._h, p, len(a)), "pkv_pool_release")
+
+    def free_count(self) -> int:
+        return int(lib().pkv_pool_free_count(self._h))
+
+    def refcount(self, page: int) -> int:
+        r = lib().pkv_pool_refcount(self._h, int(page))
+        if r < 0:
+            raise PagedKVError(r, "pkv_pool_refcount")
+        return int(r)
+
+    def lookup(self, tokens, now: float, max_pages: int = 1 << 20):
+        t, tp = self._arr(tokens if len(tokens) else [0])
+        n_max = min(max_pages, len(tokens) // self.page_size)
+        out = np.zeros(max(n_max, 1), dtype=np.int32)
+        n = lib().pkv_prefix_lookup(self._h, tp, len(tokens), float(now),
+                                    out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), int(n_max))
+        if n < 0:
+            raise PagedKVError(n, "pkv_prefix_lookup")
+        return [int(x) for x in out[:n]]
+
+    def insert(self, tokens, pages, now: float) -> int:
+        t, tp = self._arr(tokens if len(tokens) else [0])
+        a, ap = self._arr(pages if len(pages) else [0])
+        n = lib().pkv_prefix_insert(self._h, tp, len(tokens), ap, len(pages), float(now))
+        if n < 0:
+            raise PagedKVError(n, "pkv_prefix_insert")
+        return int(n)
+
+    def evict(self, now: float, ttl: float, want_free: int = 0) -> int:
+        n = lib().pkv_prefix_evict(self._h, float(now), float(ttl), int(want_free))
+        if n < 0:
+            raise PagedKVError(n, "pkv_prefix_evict")
+        return int(n)
+
+    def cache_size(self) -> int:
+        return int(lib().pkv_prefix_size(self._h))
