@@ -77,6 +77,7 @@ typedef enum {
                                    that row's output is left unwritten */
 #define PKV_DEV_TIMEOUT 0x8     /* a kernel's internal wait gave up (a bug, never expected);
                                    the outputs of that call are unspecified */
+#define PKV_DEV_BAD_POSITION 0x10 /* rope append: a position outside [0, max_pos); that row skipped */
 
 /* One layer's K (or V) page pool: contiguous
  * [num_pages, page_size, num_kv_heads, head_dim] of `dtype`. */
@@ -145,6 +146,34 @@ int pkv_pack_tick(int32_t num_seqs, const int32_t* q_lens, const int32_t* kv_len
  */
 int pkv_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int32_t num_tokens,
                   void* k_cache, void* v_cache, const pkv_cache_desc* cache, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Rotary position embedding fused into the append (Helios blog, "torch.sdpa
+ * and Flash Attention": RoPE is applied to Q and K before attention;
+ * llm-serving-engine README, component table "RoPE from scratch": cached
+ * sin/cos tables). Half-split form: for pair i < d/2 of a head row x at
+ * position p, with a = p * base^(-2i/d),
+ *   x'_i = x_i cos a - x_{i+d/2} sin a,   x'_{i+d/2} = x_{i+d/2} cos a + x_i sin a.
+ *
+ * pkv_rope_table (host): fills cos_sin[max_pos][head_dim/2][2] (float) with
+ * (cos a, sin a), computed in double. PKV_E_SHAPE unless base > 1, head_dim
+ * even >= 2, max_pos >= 1.
+ *
+ * pkv_rope_kv_append (device): for each new token t at position positions[t]
+ * (int32, device), rotates its K rows and writes them to slot slot_mapping[t]
+ * (as pkv_kv_append; a negative slot skips K and V), copies its V rows to the
+ * slot unrotated, and writes its rotated Q rows [num_tokens, num_q_heads,
+ * head_dim] to q_out (q_out may equal q: in place). cos_sin is the device copy
+ * of the table above. A position outside [0, max_pos) sets
+ * PKV_DEV_BAD_POSITION and skips that token's Q and K rows. Rotation in fp32,
+ * results rounded to the cache dtype. Errors as pkv_kv_append, plus PKV_E_SHAPE
+ * for an odd head_dim or num_q_heads < 1.
+ */
+int pkv_rope_table(double base, int32_t head_dim, int32_t max_pos, float* cos_sin);
+int pkv_rope_kv_append(const void* q, const void* k, const void* v, const int32_t* positions,
+                       const float* cos_sin, int32_t max_pos, const int64_t* slot_mapping, int32_t num_tokens,
+                       int32_t num_q_heads, void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                       void* q_out, pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * pkv_paged_attention_workspace_size — bytes of device workspace that

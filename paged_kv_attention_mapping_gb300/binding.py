@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
 
 PKV_F32, PKV_F16, PKV_BF16 = 0, 1, 2
-DEV_BAD_SLOT, DEV_BAD_LENGTHS, DEV_BAD_PAGE = 0x1, 0x2, 0x4
+DEV_BAD_SLOT, DEV_BAD_LENGTHS, DEV_BAD_PAGE, DEV_TIMEOUT, DEV_BAD_POSITION = 0x1, 0x2, 0x4, 0x8, 0x10
 
 EXPORTED = (
     "pkv_pack_tick",
@@ -42,6 +42,8 @@ EXPORTED = (
     "pkv_prefix_insert",
     "pkv_prefix_evict",
     "pkv_prefix_size",
+    "pkv_rope_table",
+    "pkv_rope_kv_append",
 )
 
 
@@ -112,6 +114,10 @@ def lib():
     L.pkv_prefix_evict.restype = ctypes.c_int
     L.pkv_prefix_size.argtypes = [vp]
     L.pkv_prefix_size.restype = ctypes.c_int
+    L.pkv_rope_table.argtypes = [ctypes.c_double, i32, i32, ctypes.POINTER(ctypes.c_float)]
+    L.pkv_rope_table.restype = ctypes.c_int
+    L.pkv_rope_kv_append.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, vp, vp, ctypes.POINTER(CacheDesc), vp, vp]
+    L.pkv_rope_kv_append.restype = ctypes.c_int
     L.pkv_version.argtypes = []
     L.pkv_version.restype = ctypes.c_char_p
     _lib = L
@@ -276,6 +282,33 @@ def paged_attention_no_alloc(q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_c
                                             _ptr(out), _ptr(lse), _stream_ptr(stream))
     _check(st, "pkv_paged_attention_no_alloc")
     return out, lse
+
+
+def rope_table(base: float, head_dim: int, max_pos: int) -> np.ndarray:
+    """Host cos/sin table [max_pos, head_dim/2, 2] float32 (pkv_rope_table)."""
+    out = np.zeros((max_pos, head_dim // 2, 2), dtype=np.float32)
+    _check(lib().pkv_rope_table(float(base), int(head_dim), int(max_pos),
+                                out.ctypes.data_as(ctypes.POINTER(ctypes.c_float))), "pkv_rope_table")
+    return out
+
+
+def rope_kv_append(q, k, v, positions, cos_sin, slot_mapping, k_cache, v_cache, q_out=None, stream=None):
+    """Rotate K and write it with V to the slots; rotate Q into q_out
+    (pkv_rope_kv_append). cos_sin: device float32 [max_pos, d/2, 2]."""
+    import torch
+    for t in (q, k, v, positions, cos_sin, slot_mapping, k_cache, v_cache):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("rope_kv_append needs contiguous CUDA tensors")
+    if positions.dtype != torch.int32 or slot_mapping.dtype != torch.int64 or cos_sin.dtype != torch.float32:
+        raise TypeError("positions int32, slot_mapping int64, cos_sin float32")
+    if q_out is None:
+        q_out = torch.empty_like(q)
+    desc = cache_desc(k_cache)
+    st = lib().pkv_rope_kv_append(_ptr(q), _ptr(k), _ptr(v), _ptr(positions), _ptr(cos_sin), int(cos_sin.shape[0]),
+                                  _ptr(slot_mapping), int(k.shape[0]), int(q.shape[1]), _ptr(k_cache),
+                                  _ptr(v_cache), ctypes.byref(desc), _ptr(q_out), _stream_ptr(stream))
+    _check(st, "pkv_rope_kv_append")
+    return q_out
 
 
 def device_status(stream=None) -> int:

@@ -154,6 +154,24 @@ extern "C" int pkv_kv_append(const void* k, const void* v, const int64_t* slot_m
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "kv_append");
 }
 
+extern "C" int pkv_rope_kv_append(const void* q, const void* k, const void* v, const int32_t* positions,
+                                  const float* cos_sin, int32_t max_pos, const int64_t* slot_mapping,
+                                  int32_t num_tokens, int32_t num_q_heads, void* k_cache, void* v_cache,
+                                  const pkv_cache_desc* cache, void* q_out, pkv_stream_t stream) {
+  int st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0 || num_q_heads < 1 || cache->head_dim % 2 != 0 || max_pos < 1) return PKV_E_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!q || !k || !v || !positions || !cos_sin || !slot_mapping || !k_cache || !v_cache || !q_out)
+    return PKV_E_NULL;
+  const DeviceFacts* f = device_facts();
+  if (!f) return PKV_E_CUDA;
+  if (!f->ok) return PKV_E_DEVICE;
+  cudaError_t e = launch_rope_append(q, k, v, positions, cos_sin, max_pos, slot_mapping, num_tokens, num_q_heads,
+                                     k_cache, v_cache, q_out, *cache, f->status, (cudaStream_t)stream);
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "rope_append");
+}
+
 static bool head_dim_supported(int d) { return d == 64 || d == 128; }
 static bool group_supported(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16; }
 

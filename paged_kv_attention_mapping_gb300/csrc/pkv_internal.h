@@ -95,6 +95,10 @@ struct AttnArgs {
 
 cudaError_t launch_append(const void* k, const void* v, const int64_t* slots, int32_t T, void* kc, void* vc,
                           const pkv_cache_desc& c, cudaStream_t s);
+cudaError_t launch_rope_append(const void* q, const void* k, const void* v, const int32_t* positions,
+                               const float* cos_sin, int32_t max_pos, const int64_t* slots, int32_t T,
+                               int32_t Hq, void* kc, void* vc, void* q_out, const pkv_cache_desc& c,
+                               int32_t* dev_status, cudaStream_t s);
 cudaError_t launch_rows(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const AttnArgs& a, cudaStream_t s);
 // Returns cudaErrorNotSupported when the shape has no tensor-core path.
