@@ -93,8 +93,11 @@ def tick_work(w):
     prefill_flops = 4 * s.head_dim * s.num_q_heads * pairs
     prefill_bytes = sum(2 * r.kv_len * row_bytes + 2 * r.q_len * s.num_q_heads * s.head_dim * elt for r in chunk)
     append_bytes = 2 * 2 * w.total_q * row_bytes         # K and V: read the rows, write the slots
+    q_bytes = w.total_q * s.num_q_heads * s.head_dim * elt
+    rope_append_bytes = append_bytes + 2 * q_bytes + 4 * w.total_q + 8 * w.total_q  # + Q read/write, positions, slots
     return dict(decode_bytes=decode_kv + decode_qo + decode_pt, decode_kv_bytes=decode_kv,
-                prefill_flops=prefill_flops, prefill_bytes=prefill_bytes, append_bytes=append_bytes)
+                prefill_flops=prefill_flops, prefill_bytes=prefill_bytes, append_bytes=append_bytes,
+                rope_append_bytes=rope_append_bytes)
 
 
 def kernel_roofline(kernel, ktimes, work, peaks, workload):
@@ -109,7 +112,8 @@ def kernel_roofline(kernel, ktimes, work, peaks, workload):
                 "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": traffic,
                 "algorithmic_per_launch": work["prefill_flops"], "avg_launch_us": avg_s * 1e6,
                 "peak_source": peaks["source"] + " bf16 burst"}
-    nbytes = {"kv_append": work["append_bytes"]}.get(kernel, work["decode_bytes"])
+    nbytes = {"kv_append": work["append_bytes"], "rope_append": work["rope_append_bytes"]}.get(kernel,
+                                                                                              work["decode_bytes"])
     ach = nbytes / avg_s / 1e9
     return {"kernel": kernel, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": ach / peaks["hbm_gbs"], "traffic": traffic, "algorithmic_per_launch": nbytes,
@@ -282,6 +286,8 @@ def main():
     ap.add_argument("--workload", default="mixed_tick", choices=list(W.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rope", action="store_true",
+                    help="rotate Q and K by position in the append (fused RoPE append) before attention")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -314,7 +320,18 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    if args.rope:
+        rope_base = 1e6 if s.head_dim == 128 else 1e4
+        tab = torch.from_numpy(binding.rope_table(rope_base, s.head_dim, w.max_kv_len + 1)).to(dev)
+        positions = i32(binding.tick_positions(packed["cu_seqlens_q"], packed["kv_lens"]))
+        q_rot = torch.empty_like(q)
+
     def step():
+        if args.rope:
+            binding.rope_kv_append(q, kn, vn, positions, tab, slots, kc, vc, q_out=q_rot)
+            binding.paged_attention(q_rot, cu, kv, pt, kc, vc, w.scale, w.max_kv_len, out=out, lse=lse,
+                                    workspace=ws)
+            return
         binding.kv_append(kn, vn, slots, kc, vc)
         binding.paged_attention(q, cu, kv, pt, kc, vc, w.scale, w.max_kv_len, out=out, lse=lse, workspace=ws)
 
@@ -437,6 +454,8 @@ def main():
         avg_s = ktimes[dom][1] / ktimes[dom][0] / 1000.0
         roof = kernel_roofline(dom, ktimes, work, peaks, args.workload)
     roof_decode = kernel_roofline("decode", ktimes, work, peaks, args.workload) if "decode" in ktimes else None
+    roof_append = (kernel_roofline("rope_append" if args.rope else "kv_append", ktimes, work, peaks, args.workload)
+                   if ("rope_append" if args.rope else "kv_append") in ktimes else None)
     decode_k = "decode" if "decode" in ktimes else ("rows" if "rows" in ktimes else None)
     decode_gbs = None
     if decode_k and work["decode_bytes"]:
@@ -451,12 +470,13 @@ def main():
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": s.dtype, "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}" + (", RoPE fused into the append" if args.rope else ""),
                    "tokens_per_step": T, "l2": "flushed between steps (512 MB write, outside the step events)",
                    "launch": "CUDA graph replay of the step (eager launches reported under eager)",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "roofline": roof,
         "roofline_decode": roof_decode,
+        "roofline_append": roof_append,
         "decode_hbm_gbs": decode_gbs,
         "kernels": per_kernel,
         "cpu_baseline": cpu,

@@ -127,6 +127,13 @@ int pkv_pack_tick(int32_t num_seqs, const int32_t* q_lens, const int32_t* kv_len
                   int32_t* order, int32_t* cu_seqlens_q, int32_t* kv_lens_out,
                   int32_t* page_tables, int64_t* slot_mapping, int32_t* total_q_out);
 
+/* pkv_tick_positions — host: position of every packed row (kv_len - q_len + i
+ * for row i of a sequence), from cu_seqlens_q[num_seqs + 1] and kv_lens
+ * (host pointers), into positions[capacity]. PKV_E_LENGTHS for q_len < 0,
+ * kv_len < q_len or cu[0] != 0; PKV_E_CAPACITY if the rows do not fit. */
+int pkv_tick_positions(int32_t num_seqs, const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                       int32_t* positions, int32_t capacity);
+
 /* ---------------------------------------------------------------------------
  * pkv_kv_append — write each new token's K and V rows into its slot
  * (Helios blog, "Prefill vs Decode": a decode step writes its new token's

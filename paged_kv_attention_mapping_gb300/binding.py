@@ -44,6 +44,7 @@ EXPORTED = (
     "pkv_prefix_size",
     "pkv_rope_table",
     "pkv_rope_kv_append",
+    "pkv_tick_positions",
 )
 
 
@@ -118,6 +119,8 @@ def lib():
     L.pkv_rope_table.restype = ctypes.c_int
     L.pkv_rope_kv_append.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, vp, vp, ctypes.POINTER(CacheDesc), vp, vp]
     L.pkv_rope_kv_append.restype = ctypes.c_int
+    L.pkv_tick_positions.argtypes = [i32, P32, P32, P32, i32]
+    L.pkv_tick_positions.restype = ctypes.c_int
     L.pkv_version.argtypes = []
     L.pkv_version.restype = ctypes.c_char_p
     _lib = L
@@ -282,6 +285,17 @@ def paged_attention_no_alloc(q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_c
                                             _ptr(out), _ptr(lse), _stream_ptr(stream))
     _check(st, "pkv_paged_attention_no_alloc")
     return out, lse
+
+
+def tick_positions(cu_seqlens_q, kv_lens) -> np.ndarray:
+    """Position of every packed row (pkv_tick_positions), host int32 array."""
+    cu = np.ascontiguousarray(cu_seqlens_q, dtype=np.int32)
+    kl = np.ascontiguousarray(kv_lens, dtype=np.int32)
+    out = np.zeros(max(int(cu[-1]), 1), dtype=np.int32)
+    P32 = ctypes.POINTER(ctypes.c_int32)
+    _check(lib().pkv_tick_positions(len(kl), cu.ctypes.data_as(P32), kl.ctypes.data_as(P32),
+                                    out.ctypes.data_as(P32), len(out)), "pkv_tick_positions")
+    return out[:int(cu[-1])]
 
 
 def rope_table(base: float, head_dim: int, max_pos: int) -> np.ndarray:

@@ -65,3 +65,23 @@ extern "C" int pkv_pack_tick(int32_t num_seqs, const int32_t* q_lens, const int3
   *total_q_out = row;
   return PKV_OK;
 }
+
+// Position of every packed row (the slot position of its new token):
+// kv_len - q_len + i for row i of a sequence (the chunk's tokens occupy the
+// last q_len positions of the context).
+extern "C" int pkv_tick_positions(int32_t num_seqs, const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                  int32_t* positions, int32_t capacity) {
+  if (num_seqs < 0) return PKV_E_SHAPE;
+  if (!cu_seqlens_q || (num_seqs > 0 && (!kv_lens || !positions))) return PKV_E_NULL;
+  if (cu_seqlens_q[0] != 0) return PKV_E_LENGTHS;
+  for (int32_t b = 0; b < num_seqs; ++b) {
+    const int32_t q = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+    if (q < 0 || kv_lens[b] < q) return PKV_E_LENGTHS;
+  }
+  if (cu_seqlens_q[num_seqs] > capacity) return PKV_E_CAPACITY;
+  for (int32_t b = 0; b < num_seqs; ++b) {
+    const int32_t q = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+    for (int32_t i = 0; i < q; ++i) positions[cu_seqlens_q[b] + i] = kv_lens[b] - q + i;
+  }
+  return PKV_OK;
+}

@@ -49,6 +49,14 @@ def test_positions_of_tick():
     assert list(positions_of_tick([0, 1, 4, 4], [10, 7, 3])) == [9, 4, 5, 6]
 
 
+def test_library_positions_match_the_oracle(lib):
+    for name in W.WORKLOADS:
+        w = W.make_workload(name)
+        p = oracle.pack_tick(*lists(w), w.shape.page_size)
+        assert np.array_equal(binding.tick_positions(p["cu_seqlens_q"], p["kv_lens"]),
+                              positions_of_tick(p["cu_seqlens_q"], p["kv_lens"]))
+
+
 # ---------------------------------------------------------------------------
 # library table (CPU)
 
