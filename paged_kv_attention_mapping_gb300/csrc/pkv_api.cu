@@ -161,9 +161,14 @@ extern "C" int pkv_rope_kv_append(const void* q, const void* k, const void* v, c
   int st = check_cache(cache);
   if (st != PKV_OK) return st;
   if (num_tokens < 0 || num_q_heads < 1 || cache->head_dim % 2 != 0 || max_pos < 1) return PKV_E_SHAPE;
+  // rotation works on 16-byte vectors of each half row
+  if ((cache->head_dim / 2 * (cache->dtype == PKV_F32 ? 4 : 2)) % 16 != 0) return PKV_E_SHAPE;
   if (num_tokens == 0) return PKV_OK;
   if (!q || !k || !v || !positions || !cos_sin || !slot_mapping || !k_cache || !v_cache || !q_out)
     return PKV_E_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(q_out) || ((uintptr_t)cos_sin & 7u))
+    return PKV_E_ALIGN;
   const DeviceFacts* f = device_facts();
   if (!f) return PKV_E_CUDA;
   if (!f->ok) return PKV_E_DEVICE;

@@ -16,7 +16,32 @@
 
 namespace pkv {
 
-// one warp per (token, head) row of Q, K or V; lanes walk the d/2 rotation pairs
+// Work items are 16-byte vectors: a Q/K item covers E = 16 / sizeof(T)
+// rotation pairs (E elements from each half of the row, with their E cos/sin
+// pairs); a V item is E elements copied. Consecutive threads take consecutive
+// vectors of a row, so every access is a full, coalesced 16-byte one.
+template <typename T>
+__device__ __forceinline__ void rotate_vec(const T* __restrict__ src, T* __restrict__ dst, int a, int half,
+                                           const float2* __restrict__ cs) {
+  constexpr int E = 16 / sizeof(T);
+  uint4 r1 = __ldg(reinterpret_cast<const uint4*>(src + a));
+  uint4 r2 = __ldg(reinterpret_cast<const uint4*>(src + a + half));
+  const T* x1 = reinterpret_cast<const T*>(&r1);
+  const T* x2 = reinterpret_cast<const T*>(&r2);
+  uint4 o1, o2;
+  T* y1 = reinterpret_cast<T*>(&o1);
+  T* y2 = reinterpret_cast<T*>(&o2);
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const float2 c = __ldg(cs + a + e);
+    const float u = to_f32(x1[e]), w = to_f32(x2[e]);
+    y1[e] = from_f32<T>(u * c.x - w * c.y);
+    y2[e] = from_f32<T>(w * c.x + u * c.y);
+  }
+  *reinterpret_cast<uint4*>(dst + a) = o1;
+  *reinterpret_cast<uint4*>(dst + a + half) = o2;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) rope_append_kernel(const T* __restrict__ q, const T* __restrict__ k,
                                                           const T* __restrict__ v, const int32_t* __restrict__ pos,
@@ -25,50 +50,44 @@ __global__ void __launch_bounds__(256) rope_append_kernel(const T* __restrict__ 
                                                           int32_t Hq, int32_t Hkv, int32_t D, int64_t pool_slots,
                                                           T* __restrict__ kc, T* __restrict__ vc, T* __restrict__ q_out,
                                                           int32_t* dev_status) {
-  const int lane = threadIdx.x & 31;
-  const int64_t rows = (int64_t)T_ * (Hq + 2 * Hkv);
+  constexpr int E = 16 / sizeof(T);
   const int half = D / 2;
-  for (int64_t row = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; row < rows;
-       row += ((int64_t)gridDim.x * blockDim.x) >> 5) {
-    const int64_t t = row / (Hq + 2 * Hkv);
-    const int h = (int)(row - t * (Hq + 2 * Hkv));
+  const int rv = half / E;                       // rotation vectors per Q/K row
+  const int cv = D / E;                          // copy vectors per V row
+  const int64_t per_token = (int64_t)(Hq + Hkv) * rv + (int64_t)Hkv * cv;
+  const int64_t total = (int64_t)T_ * per_token;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = idx / per_token;
+    int64_t r = idx - t * per_token;
     const int p = __ldg(pos + t);
-    if (h < Hq + Hkv && (p < 0 || p >= max_pos)) {
-      if (lane == 0) atomicOr(dev_status, PKV_DEV_BAD_POSITION);
-      continue;
-    }
-    if (h < Hq) {  // a query row: rotate into q_out
-      const T* src = q + (t * Hq + h) * D;
-      T* dst = q_out + (t * Hq + h) * D;
-      for (int i = lane; i < half; i += 32) {
-        const float2 c = __ldg(cs + (int64_t)p * half + i);
-        const float x1 = to_f32(src[i]), x2 = to_f32(src[i + half]);
-        dst[i] = from_f32<T>(x1 * c.x - x2 * c.y);
-        dst[i + half] = from_f32<T>(x2 * c.x + x1 * c.y);
-      }
-      continue;
-    }
     const int64_t slot = __ldg(slots + t);
-    if (slot < 0) continue;
-    if (slot >= pool_slots) {
-      if (lane == 0) atomicOr(dev_status, PKV_DEV_BAD_SLOT);
-      continue;
-    }
-    if (h < Hq + Hkv) {  // a key row: rotate into its slot
-      const int kh = h - Hq;
-      const T* src = k + (t * Hkv + kh) * D;
-      T* dst = kc + (slot * Hkv + kh) * D;
-      for (int i = lane; i < half; i += 32) {
-        const float2 c = __ldg(cs + (int64_t)p * half + i);
-        const float x1 = to_f32(src[i]), x2 = to_f32(src[i + half]);
-        dst[i] = from_f32<T>(x1 * c.x - x2 * c.y);
-        dst[i + half] = from_f32<T>(x2 * c.x + x1 * c.y);
+    if (r < (int64_t)(Hq + Hkv) * rv) {
+      const int h = (int)(r / rv);
+      const int a = (int)(r - (int64_t)h * rv) * E;
+      if (p < 0 || p >= max_pos) {
+        if (a == 0) atomicOr(dev_status, PKV_DEV_BAD_POSITION);
+        continue;
       }
-    } else {  // a value row: copied as is
-      const int vh = h - Hq - Hkv;
-      const T* src = v + (t * Hkv + vh) * D;
-      T* dst = vc + (slot * Hkv + vh) * D;
-      for (int i = lane; i < D; i += 32) dst[i] = src[i];
+      const float2* c = cs + (int64_t)p * half;
+      if (h < Hq) {
+        rotate_vec<T>(q + (t * Hq + h) * D, q_out + (t * Hq + h) * D, a, half, c);
+      } else {
+        if (slot < 0) continue;
+        if (slot >= pool_slots) {
+          if (a == 0 && h == Hq) atomicOr(dev_status, PKV_DEV_BAD_SLOT);
+          continue;
+        }
+        const int kh = h - Hq;
+        rotate_vec<T>(k + (t * Hkv + kh) * D, kc + (slot * Hkv + kh) * D, a, half, c);
+      }
+    } else {
+      r -= (int64_t)(Hq + Hkv) * rv;
+      if (slot < 0 || slot >= pool_slots) continue;
+      const int vh = (int)(r / cv);
+      const int a = (int)(r - (int64_t)vh * cv) * E;
+      *reinterpret_cast<uint4*>(vc + (slot * Hkv + vh) * D + a) =
+          __ldg(reinterpret_cast<const uint4*>(v + (t * Hkv + vh) * D + a));
     }
   }
 }
@@ -78,9 +97,11 @@ cudaError_t launch_rope_append(const void* q, const void* k, const void* v, cons
                                int32_t Hq, void* kc, void* vc, void* q_out, const pkv_cache_desc& c,
                                int32_t* dev_status, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const int64_t rows = (int64_t)T * (Hq + 2 * c.num_kv_heads);
-  int64_t blocks = (rows * 32 + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  const int E = c.dtype == PKV_F32 ? 4 : 8;
+  const int64_t items = (int64_t)T * ((int64_t)(Hq + c.num_kv_heads) * (c.head_dim / 2 / E) +
+                                      (int64_t)c.num_kv_heads * (c.head_dim / E));
+  int64_t blocks = (items + 255) / 256;
+  if (blocks > 152 * 32) blocks = 152 * 32;
   const int64_t pool_slots = (int64_t)c.num_pages * c.page_size;
   KernelTimer timer("rope_append", s);
   switch (c.dtype) {
