@@ -80,10 +80,12 @@ def load_peaks():
 # ---------------------------------------------------------------------------
 # algorithmic work of the tick (bytes and flops a perfect kernel must move/do)
 
-def tick_work(w):
+def tick_work(w, kv_elt=None):
+    """kv_elt: bytes per cache element when it differs from the q/out type (1 for an fp8 cache)."""
     s = w.shape
     elt = s.elt_bytes
-    row_bytes = s.num_kv_heads * s.head_dim * elt        # one token's K (or V) for all KV heads
+    kv_elt = kv_elt or elt
+    row_bytes = s.num_kv_heads * s.head_dim * kv_elt     # one token's K (or V) for all KV heads
     dec_rows = [r for r in w.requests if r.q_len == 1]
     chunk = [r for r in w.requests if r.q_len > 1]
     decode_kv = sum(2 * r.kv_len * row_bytes for r in dec_rows)
@@ -92,7 +94,8 @@ def tick_work(w):
     pairs = sum(r.q_len * (r.kv_len - r.q_len) + r.q_len * (r.q_len + 1) // 2 for r in chunk)
     prefill_flops = 4 * s.head_dim * s.num_q_heads * pairs
     prefill_bytes = sum(2 * r.kv_len * row_bytes + 2 * r.q_len * s.num_q_heads * s.head_dim * elt for r in chunk)
-    append_bytes = 2 * 2 * w.total_q * row_bytes         # K and V: read the rows, write the slots
+    # K and V: read the new rows (q/out type), write the slots (cache type)
+    append_bytes = 2 * w.total_q * s.num_kv_heads * s.head_dim * (elt + kv_elt)
     q_bytes = w.total_q * s.num_q_heads * s.head_dim * elt
     rope_append_bytes = append_bytes + 2 * q_bytes + 4 * w.total_q + 8 * w.total_q  # + Q read/write, positions, slots
     return dict(decode_bytes=decode_kv + decode_qo + decode_pt, decode_kv_bytes=decode_kv,
@@ -112,8 +115,8 @@ def kernel_roofline(kernel, ktimes, work, peaks, workload):
                 "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": traffic,
                 "algorithmic_per_launch": work["prefill_flops"], "avg_launch_us": avg_s * 1e6,
                 "peak_source": peaks["source"] + " bf16 burst"}
-    nbytes = {"kv_append": work["append_bytes"], "rope_append": work["rope_append_bytes"]}.get(kernel,
-                                                                                              work["decode_bytes"])
+    nbytes = {"kv_append": work["append_bytes"], "kv_append_quant": work["append_bytes"],
+              "rope_append": work["rope_append_bytes"]}.get(kernel, work["decode_bytes"])
     ach = nbytes / avg_s / 1e9
     return {"kernel": kernel, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": ach / peaks["hbm_gbs"], "traffic": traffic, "algorithmic_per_launch": nbytes,
@@ -288,6 +291,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rope", action="store_true",
                     help="rotate Q and K by position in the append (fused RoPE append) before attention")
+    ap.add_argument("--kv-fp8", action="store_true",
+                    help="e4m3 KV cache with per-KV-head scales (quantising append + fp8 attention); "
+                         "decode-only workloads")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -308,12 +314,27 @@ def main():
     kl = [r.kv_len for r in w.requests]
     pg = [r.pages for r in w.requests]
     packed = binding.pack_tick(ql, kl, pg, s.page_size, w.num_pages)
+    if args.kv_fp8 and (args.rope or any(x != 1 for x in ql)):
+        raise SystemExit("--kv-fp8 runs decode-only workloads without --rope")
     vals = W.device_values(w, dev)
     i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     cu, kv, pt = i32(packed["cu_seqlens_q"]), i32(packed["kv_lens"]), i32(packed["page_tables"])
     slots = i32(packed["slot_mapping"])
     q, kn, vn, kc, vc = vals["q"], vals["k_new"], vals["v_new"], vals["k_cache"], vals["v_cache"]
     T = w.total_q
+    if args.kv_fp8:
+        # quantise the synthetic pool once (untimed): unit-normal values, scale 4/448 per KV head
+        ks = torch.full((s.num_kv_heads,), 4.0 / 448.0, device=dev)
+        vs = torch.full((s.num_kv_heads,), 4.0 / 448.0, device=dev)
+        k8 = torch.empty(kc.shape, dtype=torch.uint8, device=dev)
+        v8 = torch.empty_like(k8)
+        n_slots = w.num_pages * s.page_size
+        all_slots = torch.arange(n_slots, dtype=torch.int64, device=dev)
+        binding.kv_append_quant(kc.reshape(n_slots, s.num_kv_heads, s.head_dim),
+                                vc.reshape(n_slots, s.num_kv_heads, s.head_dim), all_slots, k8, v8, ks, vs)
+        torch.cuda.synchronize()
+        del kc, vc
+        kc, vc = k8, v8
     out = torch.empty_like(q)
     lse = torch.empty((T, s.num_q_heads), dtype=torch.float32, device=dev)
     ws = binding.alloc_workspace(len(ql), T, s.num_q_heads, kc, w.max_kv_len)
@@ -326,14 +347,22 @@ def main():
         positions = i32(binding.tick_positions(packed["cu_seqlens_q"], packed["kv_lens"]))
         q_rot = torch.empty_like(q)
 
+    def append_attend(q_, k_, v_, slots_, cu_, kv_, pt_):
+        if args.kv_fp8:
+            binding.kv_append_quant(k_, v_, slots_, kc, vc, ks, vs)
+            binding.paged_attention_fp8(q_, cu_, kv_, pt_, kc, vc, ks, vs, w.scale, w.max_kv_len, out=out, lse=lse,
+                                        workspace=ws)
+            return
+        binding.kv_append(k_, v_, slots_, kc, vc)
+        binding.paged_attention(q_, cu_, kv_, pt_, kc, vc, w.scale, w.max_kv_len, out=out, lse=lse, workspace=ws)
+
     def step():
         if args.rope:
             binding.rope_kv_append(q, kn, vn, positions, tab, slots, kc, vc, q_out=q_rot)
             binding.paged_attention(q_rot, cu, kv, pt, kc, vc, w.scale, w.max_kv_len, out=out, lse=lse,
                                     workspace=ws)
             return
-        binding.kv_append(kn, vn, slots, kc, vc)
-        binding.paged_attention(q, cu, kv, pt, kc, vc, w.scale, w.max_kv_len, out=out, lse=lse, workspace=ws)
+        append_attend(q, kn, vn, slots, cu, kv, pt)
 
     clk = ClockSampler(local)
     clk.__enter__()
@@ -418,9 +447,7 @@ def main():
         d_q.copy_(h_q, non_blocking=True)
         d_k.copy_(h_k, non_blocking=True)
         d_v.copy_(h_v, non_blocking=True)
-        binding.kv_append(d_k, d_v, d_meta[3], kc, vc)
-        binding.paged_attention(d_q, d_meta[0], d_meta[1], d_meta[2], kc, vc, w.scale, w.max_kv_len, out=out,
-                                lse=lse, workspace=ws)
+        append_attend(d_q, d_k, d_v, d_meta[3], d_meta[0], d_meta[1], d_meta[2])
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
         torch.cuda.current_stream().synchronize()
@@ -443,7 +470,7 @@ def main():
         return 0
 
     peaks = load_peaks()
-    work = tick_work(w)
+    work = tick_work(w, kv_elt=1 if args.kv_fp8 else None)
     per_kernel = {k: {"launches": n, "avg_us": 1000.0 * t / n, "share": None} for k, (n, t) in ktimes.items()}
     tot = sum(t for _, t in ktimes.values()) or 1.0
     for k, (n, t) in ktimes.items():
@@ -454,8 +481,8 @@ def main():
         avg_s = ktimes[dom][1] / ktimes[dom][0] / 1000.0
         roof = kernel_roofline(dom, ktimes, work, peaks, args.workload)
     roof_decode = kernel_roofline("decode", ktimes, work, peaks, args.workload) if "decode" in ktimes else None
-    roof_append = (kernel_roofline("rope_append" if args.rope else "kv_append", ktimes, work, peaks, args.workload)
-                   if ("rope_append" if args.rope else "kv_append") in ktimes else None)
+    app_k = "rope_append" if args.rope else ("kv_append_quant" if args.kv_fp8 else "kv_append")
+    roof_append = kernel_roofline(app_k, ktimes, work, peaks, args.workload) if app_k in ktimes else None
     decode_k = "decode" if "decode" in ktimes else ("rows" if "rows" in ktimes else None)
     decode_gbs = None
     if decode_k and work["decode_bytes"]:
@@ -469,8 +496,10 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": s.dtype, "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}" + (", RoPE fused into the append" if args.rope else ""),
+        "vs_baseline": None, "dtype": s.dtype + ("+e4m3 cache" if args.kv_fp8 else ""), "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"
+                               + (", RoPE fused into the append" if args.rope else "")
+                               + (", e4m3 KV cache (per-KV-head scales)" if args.kv_fp8 else ""),
                    "tokens_per_step": T, "l2": "flushed between steps (512 MB write, outside the step events)",
                    "launch": "CUDA graph replay of the step (eager launches reported under eager)",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},

@@ -51,7 +51,9 @@ typedef struct CUstream_st* pkv_stream_t; /* same handle as cudaStream_t */
 typedef enum {
   PKV_F32 = 0,
   PKV_F16 = 1,
-  PKV_BF16 = 2
+  PKV_BF16 = 2,
+  PKV_FP8_E4M3 = 3 /* caches only, with per-KV-head scales (pkv_kv_append_quant,
+                      pkv_paged_attention_fp8) */
 } pkv_dtype;
 
 typedef enum {
@@ -225,6 +227,51 @@ int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, const int32_
                         const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
                         float scale, void* out, float* lse,
                         void* workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * FP8 (e4m3) KV cache. mini-vLLM, "Quantization": 8-bit weights widened
+ * before every matmul saved memory but slowed decode, and the page names a
+ * fused low-precision kernel as the missing step. Here the cache holds one
+ * byte per element and the attention kernel widens the codes in registers, so
+ * a decode step reads half the bytes of a 16-bit cache.
+ *
+ * Cache dtype PKV_FP8_E4M3: same [num_pages, page_size, num_kv_heads,
+ * head_dim] layout, one e4m3 code per element (1 sign, 4 exponent bits with
+ * bias 7, 3 mantissa bits; largest finite 448; no infinities). Element
+ * (slot, h, i) stands for code * k_scale[h] (K) or code * v_scale[h] (V);
+ * k_scale, v_scale are device float [num_kv_heads], owned by the caller,
+ * finite and > 0.
+ *
+ * pkv_kv_append_quant: as pkv_kv_append, but k, v are [num_tokens,
+ * num_kv_heads, head_dim] of src_dtype (PKV_F32/F16/BF16) and each element x
+ * is stored as e4m3(x / scale[h]): the quotient in IEEE float32 (correctly
+ * rounded), then the nearest e4m3 value, ties to even, saturating to +-448
+ * (NaN stays NaN). Bit-exact against that definition. head_dim must be a
+ * multiple of 16. Errors as pkv_kv_append; PKV_E_DTYPE unless the cache is
+ * PKV_FP8_E4M3 (pkv_kv_append and pkv_rope_kv_append answer PKV_E_DTYPE for an
+ * fp8 cache).
+ *
+ * pkv_paged_attention_fp8: as pkv_paged_attention over an fp8 cache; q and
+ * out are q_dtype (PKV_BF16 or PKV_F16), lse as there. Scores are
+ * (q . code) * k_scale[h] * scale and the output is (sum p_j code_j) *
+ * v_scale[h] / sum p_j. q is rounded to fp16 for the products with the codes
+ * (every e4m3 value is exact in fp16), so bf16 queries must lie within fp16's
+ * range. head_dim must be 128; page_size as for the 16-bit decode path. Every
+ * row (decode and chunk rows alike) runs on the TMA-staged row kernel.
+ * Errors as pkv_paged_attention, plus PKV_E_DTYPE for another cache or query
+ * type and PKV_E_NULL for missing scales. pkv_paged_attention answers
+ * PKV_E_DTYPE for an fp8 cache. The workspace size is
+ * pkv_paged_attention_workspace_size with the fp8 cache descriptor.
+ */
+int pkv_kv_append_quant(const void* k, const void* v, int32_t src_dtype, const int64_t* slot_mapping,
+                        int32_t num_tokens, void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                        const float* k_scale, const float* v_scale, pkv_stream_t stream);
+int pkv_paged_attention_fp8(const void* q, int32_t q_dtype, const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                            const int32_t* page_tables, int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                            int32_t max_pages_per_seq, int32_t max_kv_len, const void* k_cache,
+                            const void* v_cache, const pkv_cache_desc* cache, const float* k_scale,
+                            const float* v_scale, float scale, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Host page pool and prefix cache (no device work; host memory only).

@@ -16,7 +16,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
 
-PKV_F32, PKV_F16, PKV_BF16 = 0, 1, 2
+PKV_F32, PKV_F16, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2, 3
 DEV_BAD_SLOT, DEV_BAD_LENGTHS, DEV_BAD_PAGE, DEV_TIMEOUT, DEV_BAD_POSITION = 0x1, 0x2, 0x4, 0x8, 0x10
 
 EXPORTED = (
@@ -45,6 +45,8 @@ EXPORTED = (
     "pkv_rope_table",
     "pkv_rope_kv_append",
     "pkv_tick_positions",
+    "pkv_kv_append_quant",
+    "pkv_paged_attention_fp8",
 )
 
 
@@ -119,6 +121,11 @@ def lib():
     L.pkv_rope_table.restype = ctypes.c_int
     L.pkv_rope_kv_append.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, vp, vp, ctypes.POINTER(CacheDesc), vp, vp]
     L.pkv_rope_kv_append.restype = ctypes.c_int
+    L.pkv_kv_append_quant.argtypes = [vp, vp, i32, vp, i32, vp, vp, ctypes.POINTER(CacheDesc), vp, vp, vp]
+    L.pkv_kv_append_quant.restype = ctypes.c_int
+    L.pkv_paged_attention_fp8.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp,
+                                          ctypes.POINTER(CacheDesc), vp, vp, ctypes.c_float, vp, vp, vp, sz, vp]
+    L.pkv_paged_attention_fp8.restype = ctypes.c_int
     L.pkv_tick_positions.argtypes = [i32, P32, P32, P32, i32]
     L.pkv_tick_positions.restype = ctypes.c_int
     L.pkv_version.argtypes = []
@@ -182,7 +189,10 @@ def pack_tick(q_lens: Sequence[int], kv_lens: Sequence[int], pages: Sequence[Seq
 
 def _dtype_code(t) -> int:
     import torch
-    m = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
+    m = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PKV_BF16,
+         torch.uint8: PKV_FP8_E4M3}
+    if hasattr(torch, "float8_e4m3fn"):
+        m[torch.float8_e4m3fn] = PKV_FP8_E4M3
     if t.dtype not in m:
         raise TypeError(f"unsupported dtype {t.dtype}")
     return m[t.dtype]
@@ -284,6 +294,52 @@ def paged_attention_no_alloc(q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_c
                                             _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), ctypes.c_float(scale),
                                             _ptr(out), _ptr(lse), _stream_ptr(stream))
     _check(st, "pkv_paged_attention_no_alloc")
+    return out, lse
+
+
+def kv_append_quant(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, stream=None):
+    """Quantise new tokens' K/V rows to e4m3 codes of x / scale[head] and write
+    them into their slots of an fp8 cache (pkv_kv_append_quant). Caches are
+    uint8 (or float8_e4m3fn) [N, P, Hkv, d]; scales float32 [Hkv] on the device."""
+    import torch
+    for t in (k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("kv_append_quant needs contiguous CUDA tensors")
+    if slot_mapping.dtype != torch.int64 or k_scale.dtype != torch.float32 or v_scale.dtype != torch.float32:
+        raise TypeError("slot_mapping int64, scales float32")
+    desc = cache_desc(k_cache)
+    st = lib().pkv_kv_append_quant(_ptr(k), _ptr(v), _dtype_code(k), _ptr(slot_mapping), int(k.shape[0]),
+                                   _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), _ptr(k_scale), _ptr(v_scale),
+                                   _stream_ptr(stream))
+    _check(st, "pkv_kv_append_quant")
+
+
+def paged_attention_fp8(q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_cache, k_scale, v_scale, scale: float,
+                        max_kv_len: int, out=None, lse=None, workspace=None, want_lse: bool = True, stream=None):
+    """Attention over an fp8 e4m3 cache (pkv_paged_attention_fp8): q/out bf16 or
+    f16 [T, Hq, d]; caches uint8 codes [N, P, Hkv, d]; element = code * scale[head]."""
+    import torch
+    T, Hq, D = q.shape
+    B = int(cu_seqlens_q.shape[0]) - 1
+    for t in (q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_cache, k_scale, v_scale):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("paged_attention_fp8 needs contiguous CUDA tensors")
+    for t in (cu_seqlens_q, kv_lens, page_tables):
+        if t.dtype != torch.int32:
+            raise TypeError("index tensors must be int32")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(B, T, Hq, k_cache, max_kv_len)
+    desc = cache_desc(k_cache)
+    st = lib().pkv_paged_attention_fp8(_ptr(q), _dtype_code(q), _ptr(cu_seqlens_q), _ptr(kv_lens),
+                                       _ptr(page_tables), B, int(T), int(Hq), int(page_tables.shape[1]),
+                                       int(max_kv_len), _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),
+                                       _ptr(k_scale), _ptr(v_scale), ctypes.c_float(scale), _ptr(out), _ptr(lse),
+                                       _ptr(workspace), int(workspace.numel()), _stream_ptr(stream))
+    _check(st, "pkv_paged_attention_fp8")
     return out, lse
 
 

@@ -113,7 +113,7 @@ extern "C" const char* pkv_status_string(int status) {
   switch (status) {
     case PKV_OK: return "ok";
     case PKV_E_NULL: return "a required pointer is NULL";
-    case PKV_E_DTYPE: return "unknown dtype";
+    case PKV_E_DTYPE: return "unknown dtype, or one this entry point does not take";
     case PKV_E_SHAPE: return "unsupported or inconsistent sizes";
     case PKV_E_LENGTHS: return "q/kv lengths break 0 <= q_len <= kv_len";
     case PKV_E_PAGES: return "page id outside the pool or too few pages";
@@ -128,11 +128,13 @@ extern "C" const char* pkv_status_string(int status) {
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+static int elt_bytes(int dtype) { return dtype == PKV_F32 ? 4 : dtype == PKV_FP8_E4M3 ? 1 : 2; }
+
 static int check_cache(const pkv_cache_desc* c) {
   if (!c) return PKV_E_NULL;
-  if (c->dtype < PKV_F32 || c->dtype > PKV_BF16) return PKV_E_DTYPE;
+  if (c->dtype < PKV_F32 || c->dtype > PKV_FP8_E4M3) return PKV_E_DTYPE;
   if (c->num_pages < 1 || c->page_size < 1 || c->num_kv_heads < 1 || c->head_dim < 1) return PKV_E_SHAPE;
-  const int elt = c->dtype == PKV_F32 ? 4 : 2;
+  const int elt = elt_bytes(c->dtype);
   if (((int64_t)c->num_kv_heads * c->head_dim * elt) % 16 != 0) return PKV_E_SHAPE;
   if ((int64_t)c->num_pages * c->page_size > INT32_MAX) return PKV_E_SHAPE;
   return PKV_OK;
@@ -142,6 +144,7 @@ extern "C" int pkv_kv_append(const void* k, const void* v, const int64_t* slot_m
                              void* k_cache, void* v_cache, const pkv_cache_desc* cache, pkv_stream_t stream) {
   int st = check_cache(cache);
   if (st != PKV_OK) return st;
+  if (cache->dtype == PKV_FP8_E4M3) return PKV_E_DTYPE;  // pkv_kv_append_quant writes fp8 caches
   if (num_tokens < 0) return PKV_E_SHAPE;
   if (num_tokens == 0) return PKV_OK;
   if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_E_NULL;
@@ -160,6 +163,7 @@ extern "C" int pkv_rope_kv_append(const void* q, const void* k, const void* v, c
                                   const pkv_cache_desc* cache, void* q_out, pkv_stream_t stream) {
   int st = check_cache(cache);
   if (st != PKV_OK) return st;
+  if (cache->dtype == PKV_FP8_E4M3) return PKV_E_DTYPE;
   if (num_tokens < 0 || num_q_heads < 1 || cache->head_dim % 2 != 0 || max_pos < 1) return PKV_E_SHAPE;
   // rotation works on 16-byte vectors of each half row
   if ((cache->head_dim / 2 * (cache->dtype == PKV_F32 ? 4 : 2)) % 16 != 0) return PKV_E_SHAPE;
@@ -191,23 +195,28 @@ extern "C" size_t pkv_paged_attention_workspace_size(int32_t num_seqs, int32_t t
 // prefill kernel (when the shape has one); shorter ones go row by row.
 static constexpr int TC_MIN_Q = 64;
 
-extern "C" int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, const int32_t* kv_lens,
-                                   const int32_t* page_tables, int32_t num_seqs, int32_t total_q,
-                                   int32_t num_q_heads, int32_t max_pages_per_seq, int32_t max_kv_len,
-                                   const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
-                                   float scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
-                                   pkv_stream_t stream) {
+// Shared body of the attention entry points: host checks, the device plan,
+// then the kernels on `stream`. q_dtype is the q/out element type; an fp8
+// cache (cache->dtype == PKV_FP8_E4M3) comes with its per-KV-head scales.
+static int attention_impl(const void* q, int q_dtype, const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                          const int32_t* page_tables, int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                          int32_t max_pages_per_seq, int32_t max_kv_len, const void* k_cache, const void* v_cache,
+                          const pkv_cache_desc* cache, const float* k_scale, const float* v_scale, float scale,
+                          void* out, float* lse, void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
   int st = check_cache(cache);
   if (st != PKV_OK) return st;
+  const bool fp8 = cache->dtype == PKV_FP8_E4M3;
   if (num_seqs < 0 || total_q < 0 || num_q_heads < 1 || max_kv_len < 0) return PKV_E_SHAPE;
   if (num_q_heads % cache->num_kv_heads != 0) return PKV_E_SHAPE;
   if (!head_dim_supported(cache->head_dim) || !group_supported(num_q_heads / cache->num_kv_heads))
     return PKV_E_SHAPE;
+  if (fp8 && !decode_supported(PKV_FP8_E4M3, cache->head_dim, cache->page_size)) return PKV_E_SHAPE;
   if (total_q > 0 && max_pages_per_seq < 1) return PKV_E_SHAPE;
   if ((int64_t)max_pages_per_seq * cache->page_size > INT32_MAX) return PKV_E_SHAPE;
   if (total_q == 0) return PKV_OK;
   if (!q || !cu_seqlens_q || !kv_lens || !page_tables || !k_cache || !v_cache || !out || !workspace)
     return PKV_E_NULL;
+  if (fp8 && (!k_scale || !v_scale)) return PKV_E_NULL;
   if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) || ((uintptr_t)lse & 3u))
     return PKV_E_ALIGN;
   if (((uintptr_t)workspace & 255u) != 0) return PKV_E_WORKSPACE;
@@ -219,7 +228,9 @@ extern "C" int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, c
   if (!f->ok) return PKV_E_DEVICE;
   cudaStream_t s = (cudaStream_t)stream;
 
-  const bool tc = prefill_tc_supported(cache->dtype, cache->head_dim, cache->page_size) && total_q >= TC_MIN_Q;
+  // fp8 caches have no tensor-core prefill kernel yet: their chunk rows take the row path
+  const bool tc = !fp8 && prefill_tc_supported(cache->dtype, cache->head_dim, cache->page_size) &&
+                  total_q >= TC_MIN_Q;
 
   PlanArgs pa{};
   pa.cu = cu_seqlens_q;
@@ -235,7 +246,7 @@ extern "C" int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, c
   // not change with the batch it is packed into. It only grows when the
   // partial results would overflow the workspace.
   {
-    const int elt = cache->dtype == PKV_F32 ? 4 : 2;
+    const int elt = elt_bytes(cache->dtype);
     int c = (1 << 20) / (2 * cache->head_dim * elt);
     pa.chunk_min = c < 256 ? 256 : c;
   }
@@ -267,18 +278,66 @@ extern "C" int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, c
   aa.lse = lse;
   aa.ws = (char*)workspace;
   aa.lay = lay;
-  aa.dtype = cache->dtype;
+  aa.dtype = q_dtype;
+  aa.kv_dtype = cache->dtype;
+  aa.k_scale = k_scale;
+  aa.v_scale = v_scale;
   aa.num_sms = f->num_sms;
   aa.dev_status = f->status;
   if (tc) {
     e = launch_prefill_tc(aa, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill_tc");
   }
-  e = decode_supported(aa.dtype, aa.D, aa.P) ? launch_decode(aa, s) : launch_rows(aa, s);
+  e = decode_supported(aa.kv_dtype, aa.D, aa.P) ? launch_decode(aa, s) : launch_rows(aa, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode");
   e = launch_combine(aa, s);
   if (e != cudaSuccess) return cuda_fail(e, "combine");
   return PKV_OK;
+}
+
+extern "C" int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                   const int32_t* page_tables, int32_t num_seqs, int32_t total_q,
+                                   int32_t num_q_heads, int32_t max_pages_per_seq, int32_t max_kv_len,
+                                   const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                                   float scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                   pkv_stream_t stream) {
+  if (cache && cache->dtype == PKV_FP8_E4M3) return PKV_E_DTYPE;  // fp8 caches: pkv_paged_attention_fp8
+  return attention_impl(q, cache ? cache->dtype : 0, cu_seqlens_q, kv_lens, page_tables, num_seqs, total_q,
+                        num_q_heads, max_pages_per_seq, max_kv_len, k_cache, v_cache, cache, nullptr, nullptr, scale,
+                        out, lse, workspace, workspace_bytes, stream);
+}
+
+extern "C" int pkv_paged_attention_fp8(const void* q, int32_t q_dtype, const int32_t* cu_seqlens_q,
+                                       const int32_t* kv_lens, const int32_t* page_tables, int32_t num_seqs,
+                                       int32_t total_q, int32_t num_q_heads, int32_t max_pages_per_seq,
+                                       int32_t max_kv_len, const void* k_cache, const void* v_cache,
+                                       const pkv_cache_desc* cache, const float* k_scale, const float* v_scale,
+                                       float scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                       pkv_stream_t stream) {
+  if (!cache) return PKV_E_NULL;
+  if (cache->dtype != PKV_FP8_E4M3 || (q_dtype != PKV_BF16 && q_dtype != PKV_F16)) return PKV_E_DTYPE;
+  return attention_impl(q, q_dtype, cu_seqlens_q, kv_lens, page_tables, num_seqs, total_q, num_q_heads,
+                        max_pages_per_seq, max_kv_len, k_cache, v_cache, cache, k_scale, v_scale, scale, out, lse,
+                        workspace, workspace_bytes, stream);
+}
+
+extern "C" int pkv_kv_append_quant(const void* k, const void* v, int32_t src_dtype, const int64_t* slot_mapping,
+                                   int32_t num_tokens, void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                                   const float* k_scale, const float* v_scale, pkv_stream_t stream) {
+  int st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (cache->dtype != PKV_FP8_E4M3 || src_dtype < PKV_F32 || src_dtype > PKV_BF16) return PKV_E_DTYPE;
+  if (num_tokens < 0 || cache->head_dim % 16 != 0) return PKV_E_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale) return PKV_E_NULL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) || ((uintptr_t)slot_mapping & 7u))
+    return PKV_E_ALIGN;
+  const DeviceFacts* f = device_facts();
+  if (!f) return PKV_E_CUDA;
+  if (!f->ok) return PKV_E_DEVICE;
+  cudaError_t e = launch_append_quant(k, v, src_dtype, slot_mapping, num_tokens, k_cache, v_cache, *cache, k_scale,
+                                      v_scale, f->status, (cudaStream_t)stream);
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "kv_append_quant");
 }
 
 extern "C" int pkv_get_device_status(int32_t* code, pkv_stream_t stream) {

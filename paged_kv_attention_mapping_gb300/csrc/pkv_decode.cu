@@ -55,6 +55,8 @@ struct DecParams {
   float* part_o;
   float* part_lse;
   int32_t* dev_status;
+  const float* k_scale;  // fp8 caches: dequantisation scale per KV head (else null)
+  const float* v_scale;
 };
 
 struct Item {
@@ -160,9 +162,26 @@ __device__ __forceinline__ uint32_t pack2h(float a, float b) {
   }
 }
 
-template <typename T, int D, int G>
+__device__ __forceinline__ uint32_t ld_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_u8(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+// two e4m3 codes (low byte first) -> two fp16 values packed (low half first)
+__device__ __forceinline__ uint32_t fp8x2_to_h2(uint32_t codes) {
+  uint32_t out;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"((uint16_t)codes));
+  return out;
+}
+
+template <typename TKV, int D, int G>
 struct DCfg {
-  static constexpr int ELT = sizeof(T);
+  static constexpr int ELT = sizeof(TKV);
   static constexpr int ROW_BYTES = D * ELT;            // one key of one KV head
   static constexpr int ATOMS = ROW_BYTES / 128;        // 128-byte swizzle atoms per key row
   static constexpr int ATOM_ELEMS = 128 / ELT;
@@ -184,10 +203,14 @@ __device__ __forceinline__ uint32_t sw_addr(uint32_t tile_base, int row, int byt
   return tile_base + atom * (BT * 128) + row * 128 + ((ch ^ (row & 7)) << 4) + (byte_off & 15);
 }
 
-template <typename T, int D, int G>
+// T: query/output element type; TKV: cache element type (T, or uint8_t for an
+// fp8 e4m3 cache, dequantised to fp16 in registers for the mma.sync path).
+template <typename T, typename TKV, int D, int G>
 __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
     decode_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv, DecParams p) {
-  using C = DCfg<T, D, G>;
+  using C = DCfg<TKV, D, G>;
+  constexpr bool FP8 = std::is_same<TKV, uint8_t>::value;
+  using TM = typename std::conditional<FP8, __half, T>::type;   // mma operand type
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   unsigned char* sStage = sm;
@@ -343,7 +366,7 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
     return __all_sync(0xffffffffu, ok);
   };
   const uint32_t stage0 = smem_u32(sStage);
-  constexpr bool MMA = C::ELT == 2;
+  constexpr bool MMA = C::ELT == 2 || FP8;
   const int grp = lane >> 2, tig = lane & 3;   // mma fragment coordinates
   for (uint32_t it = 0;; ++it) {
     const int slot = it & 1;
@@ -367,7 +390,13 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
       for (int kk = 0; kk < D / 16; ++kk) {
         const int c0 = kk * 16 + tig * 2;
         auto ld2 = [&](int row, int col) -> uint32_t {
-          return row < G ? *reinterpret_cast<const uint32_t*>(qg + row * D + col) : 0u;
+          if (row >= G) return 0u;
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(qg + row * D + col);
+          if constexpr (FP8 && !std::is_same<T, __half>::value) {
+            return pack2h<__half>(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));  // bf16 -> fp16
+          } else {
+            return w;
+          }
         };
         qa[kk][0] = ld2(grp, c0);
         qa[kk][1] = ld2(grp + 8, c0);
@@ -375,6 +404,8 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
         qa[kk][3] = ld2(grp + 8, c0 + 8);
       }
       constexpr bool HI = G > 8;                 // rows grp + 8 are real heads
+      // an fp8 cache stores K / k_scale: fold the scale into the score scale
+      const float qk_scale = FP8 ? p.scale_log2 * __ldg(p.k_scale + item.kvh) : p.scale_log2;
       float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
       float o[D / 8][4];
 #pragma unroll
@@ -413,9 +444,20 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
               const int krow = warp * 16 + nt * 8 + (lane & 7);
               const int dim = (kk + (mtx >> 1)) * 16 + (mtx & 1) * 8;
               uint32_t b0, b1, b2, b3;
-              ldsm_x4(sw_addr<C::ATOMS>(kbase, krow, dim * 2), b0, b1, b2, b3);
-              mma16816<T>(s[nt], qa[kk], b0, b1);
-              mma16816<T>(s[nt], qa[kk + 1], b2, b3);
+              if constexpr (FP8) {
+                // lane (grp, tig) needs bytes 2*tig, 2*tig+1 and +8 of each 16-dim step of key grp
+                const int kr = warp * 16 + nt * 8 + grp;
+                b0 = fp8x2_to_h2(ld_u16(sw_addr<C::ATOMS>(kbase, kr, kk * 16 + tig * 2)));
+                b1 = fp8x2_to_h2(ld_u16(sw_addr<C::ATOMS>(kbase, kr, kk * 16 + tig * 2 + 8)));
+                b2 = fp8x2_to_h2(ld_u16(sw_addr<C::ATOMS>(kbase, kr, kk * 16 + 16 + tig * 2)));
+                b3 = fp8x2_to_h2(ld_u16(sw_addr<C::ATOMS>(kbase, kr, kk * 16 + 16 + tig * 2 + 8)));
+                (void)krow;
+                (void)dim;
+              } else {
+                ldsm_x4(sw_addr<C::ATOMS>(kbase, krow, dim * 2), b0, b1, b2, b3);
+              }
+              mma16816<TM>(s[nt], qa[kk], b0, b1);
+              mma16816<TM>(s[nt], qa[kk + 1], b2, b3);
             }
           }
           // online softmax over the warp's keys (rows: head grp, and grp + 8)
@@ -428,7 +470,7 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 const int key = nt * 8 + tig * 2 + e;
-                float v = s[nt][hr * 2 + e] * p.scale_log2;
+                float v = s[nt][hr * 2 + e] * qk_scale;
                 v = key < nvalid ? v : -INFINITY;
                 s[nt][hr * 2 + e] = v;
                 mx = fmaxf(mx, v);
@@ -460,20 +502,31 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
           }
           // P as the A operand: keys 0-7 from n-tile 0, keys 8-15 from n-tile 1
           uint32_t pa[4];
-          pa[0] = pack2h<T>(pv[0][0], pv[0][1]);
-          pa[1] = pack2h<T>(pv[0][2], pv[0][3]);
-          pa[2] = pack2h<T>(pv[1][0], pv[1][1]);
-          pa[3] = pack2h<T>(pv[1][2], pv[1][3]);
+          pa[0] = pack2h<TM>(pv[0][0], pv[0][1]);
+          pa[1] = pack2h<TM>(pv[0][2], pv[0][3]);
+          pa[2] = pack2h<TM>(pv[1][0], pv[1][1]);
+          pa[3] = pack2h<TM>(pv[1][2], pv[1][3]);
           // O += P V over the warp's 16 keys
 #pragma unroll
           for (int nd = 0; nd < D / 8; nd += 2) {
-            const int mtx = lane >> 3;
-            const int vrow = warp * 16 + (mtx & 1) * 8 + (lane & 7);
-            const int dim = (nd + (mtx >> 1)) * 8;
             uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(sw_addr<C::ATOMS>(vbase, vrow, dim * 2), b0, b1, b2, b3);
-            mma16816<T>(o[nd], pa, b0, b1);
-            mma16816<T>(o[nd + 1], pa, b2, b3);
+            if constexpr (FP8) {
+              // lane (grp, tig) needs dim nd*8+grp of keys 2*tig, 2*tig+1 (b0) and +8 (b1)
+              const int k0 = warp * 16 + tig * 2;
+              auto vb = [&](int key, int dimv) -> uint32_t { return ld_u8(sw_addr<C::ATOMS>(vbase, key, dimv)); };
+              const int d0 = nd * 8 + grp, d1 = d0 + 8;
+              b0 = fp8x2_to_h2(vb(k0, d0) | (vb(k0 + 1, d0) << 8));
+              b1 = fp8x2_to_h2(vb(k0 + 8, d0) | (vb(k0 + 9, d0) << 8));
+              b2 = fp8x2_to_h2(vb(k0, d1) | (vb(k0 + 1, d1) << 8));
+              b3 = fp8x2_to_h2(vb(k0 + 8, d1) | (vb(k0 + 9, d1) << 8));
+            } else {
+              const int mtx = lane >> 3;
+              const int vrow = warp * 16 + (mtx & 1) * 8 + (lane & 7);
+              const int dim = (nd + (mtx >> 1)) * 8;
+              ldsm_x4_t(sw_addr<C::ATOMS>(vbase, vrow, dim * 2), b0, b1, b2, b3);
+            }
+            mma16816<TM>(o[nd], pa, b0, b1);
+            mma16816<TM>(o[nd + 1], pa, b2, b3);
           }
           if (nvalid < 16) fence_proxy_async_smem();   // our zeroing before the next TMA write
         }
@@ -645,6 +698,7 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
           ov += sMergeO[(w * G + h) * D + (e - h * D)] * sc;
         }
         ov /= l;
+        if constexpr (FP8) ov *= __ldg(p.v_scale + item.kvh);   // the cache stores V / v_scale
         const float lse_n = (m + __log2f(l)) * LN2;
         if (item.nsplit == 1) {
           ((T*)p.out)[((int64_t)item.r * p.Hq + item.kvh * G) * D + e] = from_f32<T>(ov);
@@ -662,18 +716,20 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
   }
 }
 
-template <typename T, int D, int G>
+template <typename T, typename TKV, int D, int G>
 cudaError_t launch_dec(const AttnArgs& a, cudaStream_t s) {
-  using C = DCfg<T, D, G>;
+  using C = DCfg<TKV, D, G>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(decode_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    attr_err = cudaFuncSetAttribute(decode_kernel<T, TKV, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const CUtensorMapDataType dt = std::is_same<T, float>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                 : std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                                  : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType dt = std::is_same<TKV, float>::value    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : std::is_same<TKV, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                 : std::is_same<TKV, uint8_t>::value ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int box_rows = a.P >= BT ? BT : a.P;
   CUtensorMap mk, mv;
   if (!make_map_boxed(&mk, a.k_cache, dt, C::ELT, D, a.Hkv, (int64_t)a.num_pages * a.P, C::ATOM_ELEMS, box_rows) ||
@@ -700,39 +756,45 @@ cudaError_t launch_dec(const AttnArgs& a, cudaStream_t s) {
   p.part_o = (float*)(a.ws + a.lay.part_o);
   p.part_lse = (float*)(a.ws + a.lay.part_lse);
   p.dev_status = a.dev_status;
-  decode_kernel<T, D, G><<<a.num_sms * CTAS_PER_SM, NTHREADS, C::SMEM, s>>>(mk, mv, p);
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
+  decode_kernel<T, TKV, D, G><<<a.num_sms * CTAS_PER_SM, NTHREADS, C::SMEM, s>>>(mk, mv, p);
   return cudaGetLastError();
 }
 
-template <typename T, int D>
+template <typename T, typename TKV, int D>
 cudaError_t launch_dec_g(const AttnArgs& a, cudaStream_t s) {
   switch (a.Hq / a.Hkv) {
-    case 1: return launch_dec<T, D, 1>(a, s);
-    case 2: return launch_dec<T, D, 2>(a, s);
-    case 4: return launch_dec<T, D, 4>(a, s);
-    case 8: return launch_dec<T, D, 8>(a, s);
-    case 16: return launch_dec<T, D, 16>(a, s);
+    case 1: return launch_dec<T, TKV, D, 1>(a, s);
+    case 2: return launch_dec<T, TKV, D, 2>(a, s);
+    case 4: return launch_dec<T, TKV, D, 4>(a, s);
+    case 8: return launch_dec<T, TKV, D, 8>(a, s);
+    case 16: return launch_dec<T, TKV, D, 16>(a, s);
     default: return cudaErrorNotSupported;
   }
 }
 
 template <typename T>
 cudaError_t launch_dec_d(const AttnArgs& a, cudaStream_t s) {
-  return a.D == 64 ? launch_dec_g<T, 64>(a, s) : launch_dec_g<T, 128>(a, s);
+  return a.D == 64 ? launch_dec_g<T, T, 64>(a, s) : launch_dec_g<T, T, 128>(a, s);
 }
 
 }  // namespace
 
 bool decode_supported(int dtype, int D, int P) {
-  (void)dtype;
   if (D != 64 && D != 128) return false;
+  if (dtype == PKV_FP8_E4M3 && D != 128) return false;   // fp8 rows must fill a 128-byte swizzle atom
   if (P % BT == 0) return true;
   return P >= 8 && P % 8 == 0 && BT % P == 0;
 }
 
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t s) {
-  if (!decode_supported(a.dtype, a.D, a.P)) return cudaErrorNotSupported;
+  if (!decode_supported(a.kv_dtype, a.D, a.P)) return cudaErrorNotSupported;
   KernelTimer timer("decode", s);
+  if (a.kv_dtype == PKV_FP8_E4M3) {
+    return a.dtype == PKV_F16 ? launch_dec_g<__half, uint8_t, 128>(a, s)
+                              : launch_dec_g<__nv_bfloat16, uint8_t, 128>(a, s);
+  }
   switch (a.dtype) {
     case PKV_F32: return launch_dec_d<float>(a, s);
     case PKV_F16: return launch_dec_d<__half>(a, s);

@@ -88,13 +88,20 @@ struct AttnArgs {
   float* lse;
   char* ws;
   PlanLayout lay;
-  int dtype;
+  int dtype;     // q / out element type
   int num_sms;
   int32_t* dev_status;
+  int kv_dtype = -1;               // cache element type (the q type unless an fp8 cache)
+  const float* k_scale = nullptr;  // fp8 caches: per-KV-head scales (device)
+  const float* v_scale = nullptr;
 };
 
 cudaError_t launch_append(const void* k, const void* v, const int64_t* slots, int32_t T, void* kc, void* vc,
                           const pkv_cache_desc& c, cudaStream_t s);
+// e4m3 cache: codes of x / scale[kv head], sources of type src_dtype (f32/f16/bf16).
+cudaError_t launch_append_quant(const void* k, const void* v, int src_dtype, const int64_t* slots, int32_t T,
+                                void* kc, void* vc, const pkv_cache_desc& c, const float* k_scale,
+                                const float* v_scale, int32_t* dev_status, cudaStream_t s);
 cudaError_t launch_rope_append(const void* q, const void* k, const void* v, const int32_t* positions,
                                const float* cos_sin, int32_t max_pos, const int64_t* slots, int32_t T,
                                int32_t Hq, void* kc, void* vc, void* q_out, const pkv_cache_desc& c,

@@ -71,7 +71,7 @@ extern "C" int pkv_paged_attention_no_alloc(const void* q, const int32_t* cu_seq
                                             const void* k_cache, const void* v_cache, const pkv_cache_desc* c,
                                             float scale, void* out, float* lse, pkv_stream_t stream) {
   if (!c) return PKV_E_NULL;
-  if (c->dtype < PKV_F32 || c->dtype > PKV_BF16) return PKV_E_DTYPE;
+  if (c->dtype < PKV_F32 || c->dtype > PKV_BF16) return PKV_E_DTYPE;   // fp8 caches: pkv_paged_attention_fp8
   if (c->num_pages < 1 || c->page_size < 1 || c->num_kv_heads < 1 || c->head_dim < 1) return PKV_E_SHAPE;
   const int elt = c->dtype == PKV_F32 ? 4 : 2;
   if (((int64_t)c->num_kv_heads * c->head_dim * elt) % 16 != 0) return PKV_E_SHAPE;
@@ -157,6 +157,7 @@ extern "C" int pkv_paged_attention_no_alloc(const void* q, const int32_t* cu_seq
   aa.ws = ws;
   aa.lay = lay;
   aa.dtype = c->dtype;
+  aa.kv_dtype = c->dtype;
   aa.num_sms = su->num_sms;
   aa.dev_status = status;
   if (tc && launch_prefill_tc(aa, s) != cudaSuccess) return PKV_E_CUDA;

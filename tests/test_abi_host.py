@@ -23,7 +23,7 @@ def lib():
 def header_functions():
     text = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pkv_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_library_exports_every_declared_call(lib):
