@@ -51,6 +51,7 @@ struct DecParams {
   float* lse;
   int32_t* ctrl;
   const int32_t* item_begin;
+  const int32_t* row_seq;
   const int32_t* part_begin;
   float* part_o;
   float* part_lse;
@@ -115,13 +116,26 @@ __device__ __forceinline__ bool wait_flag(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-__device__ __forceinline__ int upper_bound_c(const int32_t* a, int n, int x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(a + mid) <= x) lo = mid + 1; else hi = mid;
+// First index i in [0, n) with a[i] > x (n if none) for a non-decreasing a,
+// searched by the whole warp: each round probes 32 evenly spaced entries in
+// one load, so n entries take about log32(n) dependent loads. Same result in
+// every lane.
+__device__ __forceinline__ int warp_upper_bound(const int32_t* a, int n, int x, int lane) {
+  int lo = 0, hi = n;   // the answer lies in [lo, hi]
+  while (hi - lo > 32) {
+    const int step = (hi - lo + 31) / 32;
+    const int idx = lo + lane * step;
+    const bool le = idx < hi && __ldg(a + idx) <= x;
+    const int c = __popc(__ballot_sync(0xffffffffu, le));   // probes 0 .. c-1 are <= x
+    if (c == 0) return lo;
+    const int nlo = lo + (c - 1) * step + 1;
+    const int nhi = lo + c * step;
+    lo = nlo;
+    hi = nhi < hi ? nhi : hi;
   }
-  return lo;
+  const int idx = lo + lane;
+  const bool le = idx < hi && __ldg(a + idx) <= x;
+  return lo + __popc(__ballot_sync(0xffffffffu, le));
 }
 
 // --- mma.sync m16n8k16 helpers (16-bit A/B, fp32 accumulators) -------------------
@@ -134,6 +148,12 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
+}
+// transpose of an 8x8 matrix of 16-bit values held in mma fragment layout
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
 }
 template <typename T>
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -162,16 +182,6 @@ __device__ __forceinline__ uint32_t pack2h(float a, float b) {
   }
 }
 
-__device__ __forceinline__ uint32_t ld_u16(uint32_t addr) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint32_t ld_u8(uint32_t addr) {
-  uint16_t v;
-  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
-  return v;
-}
 // two e4m3 codes (low byte first) -> two fp16 values packed (low half first)
 __device__ __forceinline__ uint32_t fp8x2_to_h2(uint32_t codes) {
   uint32_t out;
@@ -187,9 +197,13 @@ struct DCfg {
   static constexpr int ATOM_ELEMS = 128 / ELT;
   static constexpr int TILE_BYTES = BT * ROW_BYTES;    // K (or V) tile
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int NST = STAGE_BYTES <= 32768 ? 3 : 2;
   static constexpr int Q_BYTES = G * D * 4;
   static constexpr int MERGE_BYTES = NCW * G * D * 4 + NCW * G * 8;
+  // Stages: enough bytes in flight to cover HBM latency. Small stages (fp8,
+  // head_dim 64) get as many as fit two CTAs per SM, up to 6.
+  static constexpr int BASE_NST = STAGE_BYTES <= 32768 ? 3 : 2;
+  static constexpr int FIT_NST = (112 * 1024 - Q_BYTES - MERGE_BYTES - 1024) / STAGE_BYTES;
+  static constexpr int NST = FIT_NST > BASE_NST ? (FIT_NST < 6 ? FIT_NST : 6) : BASE_NST;
   static constexpr int SMEM = NST * STAGE_BYTES + Q_BYTES + MERGE_BYTES + 1024;
   static constexpr int DPL = D / 32;                   // PV: dims per lane
   static_assert(ROW_BYTES % 128 == 0, "key rows must be whole swizzle atoms");
@@ -253,43 +267,61 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
       if (!__all_sync(0xffffffffu, wait_flag(&bar_iempty[slot], ((it >> 1) & 1) ^ 1, &s_abort, p.ctrl,
                                              p.dev_status)))
         break;
+      // next item, decoded by the whole warp (few dependent loads)
+      int i = 0;
+      if (lane == 0) i = s_abort ? n_items : atomicAdd(&p.ctrl[CTRL_ITEM_NEXT], 1);
+      i = __shfl_sync(0xffffffffu, i, 0);
       Item item;
       item.valid = 0;
+      if (i < n_items) {
+        const int r = warp_upper_bound(p.item_begin, p.T + 1, i, lane) - 1;
+        const int b0 = __ldg(p.item_begin + r);
+        const int b1 = __ldg(p.item_begin + r + 1);
+        const int b = max(0, __ldg(p.row_seq + r));   // every row with items has its sequence here
+        const int c0 = __ldg(p.cu + b);
+        const int qlen = __ldg(p.cu + b + 1) - c0;
+        const int L = __ldg(p.kv_lens + b);
+        item.local = i - b0;
+        item.nsplit = (b1 - b0) / p.Hkv;
+        item.kvh = item.local / item.nsplit;
+        const int sp = item.local - item.kvh * item.nsplit;
+        const int limit = L - qlen + (r - c0) + 1;
+        item.r = r;
+        item.b = b;
+        item.k0 = sp * Cchunk;
+        item.k1 = min(limit, item.k0 + Cchunk);
+        item.n_tiles = (item.k1 - item.k0 + BT - 1) / BT;
+        item.valid = 1;
+      }
       if (lane == 0) {
-        const int i = s_abort ? n_items : atomicAdd(&p.ctrl[CTRL_ITEM_NEXT], 1);
-        if (i < n_items) {
-          const int r = upper_bound_c(p.item_begin, p.T + 1, i) - 1;
-          const int b0 = __ldg(p.item_begin + r);
-          item.local = i - b0;
-          item.nsplit = (__ldg(p.item_begin + r + 1) - b0) / p.Hkv;
-          item.kvh = item.local / item.nsplit;
-          const int sp = item.local - item.kvh * item.nsplit;
-          const int b = upper_bound_c(p.cu, p.B + 1, r) - 1;
-          const int c0 = __ldg(p.cu + b);
-          const int qlen = __ldg(p.cu + b + 1) - c0;
-          const int L = __ldg(p.kv_lens + b);
-          const int limit = L - qlen + (r - c0) + 1;
-          item.r = r;
-          item.b = b;
-          item.k0 = sp * Cchunk;
-          item.k1 = min(limit, item.k0 + Cchunk);
-          item.n_tiles = (item.k1 - item.k0 + BT - 1) / BT;
-          item.valid = 1;
-        }
         s_item[slot] = item;
         s_bad[slot] = 0;
         mbar_arrive(&bar_ifull[slot]);
       }
-      item.valid = __shfl_sync(0xffffffffu, item.valid, 0);
       if (!item.valid) break;
-      item.b = __shfl_sync(0xffffffffu, item.b, 0);
-      item.kvh = __shfl_sync(0xffffffffu, item.kvh, 0);
-      item.k0 = __shfl_sync(0xffffffffu, item.k0, 0);
-      item.k1 = __shfl_sync(0xffffffffu, item.k1, 0);
-      item.n_tiles = __shfl_sync(0xffffffffu, item.n_tiles, 0);
+      // the item's page ids, 32 logical pages per coalesced warp load; lane j
+      // holds page wb + j (-1 past the item's last page)
       const int32_t* pt = p.page_tables + (int64_t)item.b * p.max_pages;
+      const int lp_last = (item.k1 - 1) / p.P;
+      int wb = item.k0 / p.P;
+      int pg = wb + lane <= lp_last ? __ldg(pt + wb + lane) : -1;
+      const int per = p.P >= BT ? 1 : BT / p.P;   // pages per tile (at most BT / 8)
       bool ok = true;
       for (int t = 0; t < item.n_tiles; ++t) {
+        const int kb = item.k0 + t * BT;
+        const int lp0 = kb / p.P;
+        const int npg = p.P >= BT ? 1 : min(per, (item.k1 - kb + p.P - 1) / p.P);
+        if (lp0 + npg - 1 >= wb + 32) {   // next window (warp-uniform)
+          wb = lp0;
+          pg = wb + lane <= lp_last ? __ldg(pt + wb + lane) : -1;
+        }
+        int page[BT / 8];
+        bool bad = false;
+#pragma unroll
+        for (int pp = 0; pp < BT / 8; ++pp) {
+          page[pp] = __shfl_sync(0xffffffffu, pg, (lp0 + pp - wb) & 31);
+          if (pp < npg) bad |= page[pp] < 0 || page[pp] >= p.num_pages;
+        }
         const uint32_t st = stage_use % C::NST, round = stage_use / C::NST;
         ++stage_use;
         if (!__all_sync(0xffffffffu, wait_flag(&bar_empty[st], (round & 1) ^ 1, &s_abort, p.ctrl, p.dev_status))) {
@@ -299,44 +331,29 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
         if (lane == 0) {
           unsigned char* kdst = sStage + st * C::STAGE_BYTES;
           unsigned char* vdst = kdst + C::TILE_BYTES;
-          const int kb = item.k0 + t * BT;
-          if (p.P >= BT) {
-            const int lp = kb / p.P;
-            const int page = __ldg(pt + lp);
-            if (page < 0 || page >= p.num_pages) {
-              s_bad[slot] = 1;
-              mbar_arrive(&bar_full[st]);
-            } else {
-              const int row = page * p.P + (kb - lp * p.P);
-              mbar_arrive_expect_tx(&bar_full[st], 2 * C::TILE_BYTES);
+          if (bad) {
+            s_bad[slot] = 1;
+            mbar_arrive(&bar_full[st]);
+          } else if (p.P >= BT) {
+            const int row = page[0] * p.P + (kb - lp0 * p.P);
+            mbar_arrive_expect_tx(&bar_full[st], 2 * C::TILE_BYTES);
 #pragma unroll
-              for (int a = 0; a < C::ATOMS; ++a) {
-                tma_load_3d(kdst + a * BT * 128, &mk, &bar_full[st], a * C::ATOM_ELEMS, item.kvh, row);
-                tma_load_3d(vdst + a * BT * 128, &mv, &bar_full[st], a * C::ATOM_ELEMS, item.kvh, row);
-              }
+            for (int a = 0; a < C::ATOMS; ++a) {
+              tma_load_3d(kdst + a * BT * 128, &mk, &bar_full[st], a * C::ATOM_ELEMS, item.kvh, row);
+              tma_load_3d(vdst + a * BT * 128, &mv, &bar_full[st], a * C::ATOM_ELEMS, item.kvh, row);
             }
           } else {
-            const int per = BT / p.P;
-            const int lp0 = kb / p.P;
-            const int cnt = min(per, (item.k1 - kb + p.P - 1) / p.P);
-            bool bad = false;
-            for (int pp = 0; pp < cnt; ++pp) {
-              const int page = __ldg(pt + lp0 + pp);
-              bad |= page < 0 || page >= p.num_pages;
-            }
-            if (bad) {
-              s_bad[slot] = 1;
-              mbar_arrive(&bar_full[st]);
-            } else {
-              mbar_arrive_expect_tx(&bar_full[st], (uint32_t)(2 * cnt * p.P * C::ROW_BYTES));
-              for (int pp = 0; pp < cnt; ++pp) {
-                const int row = __ldg(pt + lp0 + pp) * p.P;
+            mbar_arrive_expect_tx(&bar_full[st], (uint32_t)(2 * npg * p.P * C::ROW_BYTES));
+#pragma unroll
+            for (int pp = 0; pp < BT / 8; ++pp) {
+              if (pp < npg) {
+                const int row = page[pp] * p.P;
 #pragma unroll
                 for (int a = 0; a < C::ATOMS; ++a) {
-                  tma_load_3d(kdst + a * BT * 128 + pp * p.P * 128, &mk, &bar_full[st], a * C::ATOM_ELEMS, item.kvh,
-                              row);
-                  tma_load_3d(vdst + a * BT * 128 + pp * p.P * 128, &mv, &bar_full[st], a * C::ATOM_ELEMS, item.kvh,
-                              row);
+                  tma_load_3d(kdst + a * BT * 128 + pp * p.P * 128, &mk, &bar_full[st], a * C::ATOM_ELEMS,
+                              item.kvh, row);
+                  tma_load_3d(vdst + a * BT * 128 + pp * p.P * 128, &mv, &bar_full[st], a * C::ATOM_ELEMS,
+                              item.kvh, row);
                 }
               }
             }
@@ -367,6 +384,9 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
   };
   const uint32_t stage0 = smem_u32(sStage);
   constexpr bool MMA = C::ELT == 2 || FP8;
+  // keys as the M rows (S^T = K Q^T, O^T = V^T P^T): one n-tile of 8 holds the
+  // whole group when G <= 8, half the MMAs of heads-as-rows
+  constexpr bool KM = MMA && G <= 8;
   const int grp = lane >> 2, tig = lane & 3;   // mma fragment coordinates
   for (uint32_t it = 0;; ++it) {
     const int slot = it & 1;
@@ -382,13 +402,183 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
     if (!cw_sync()) break;
     bool ok = true;
     bool bad = false;
-    if constexpr (MMA) {
-      // ------------------------------------------------ tensor-core (mma.sync) path
+    if constexpr (KM) {
+      // ------------------------------------------------ tensor cores, keys as rows
+      // Q^T as the B operand: column n = head grp (zero for grp >= G). For fp8
+      // the contraction index of each 16-dim block is permuted so that k slots
+      // (2tig, 2tig+1 | 2tig+8, 2tig+9) hold dims (4tig, 4tig+1 | 4tig+2, 4tig+3),
+      // the four bytes one ldmatrix lane receives from a key row.
+      uint32_t qb[D / 16][2];
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int c0 = kk * 16 + (FP8 ? tig * 4 : tig * 2);
+        constexpr int HI_K = FP8 ? 2 : 8;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          uint32_t w = 0u;
+          if (grp < G) {
+            w = *reinterpret_cast<const uint32_t*>(qg + grp * D + c0 + u * HI_K);
+            if constexpr (FP8 && !std::is_same<T, __half>::value)
+              w = pack2h<__half>(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));  // bf16 -> fp16
+          }
+          qb[kk][u] = w;
+        }
+      }
+      // an fp8 cache stores K / k_scale: fold the scale into the score scale
+      const float qk_scale = FP8 ? p.scale_log2 * __ldg(p.k_scale + item.kvh) : p.scale_log2;
+      // per lane: heads 2tig, 2tig+1; O^T tiles: rows = dims, columns = heads
+      float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
+      float o[D / 16][4];
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      for (int t = 0; t < item.n_tiles; ++t) {
+        const uint32_t st = stage_use % C::NST, round = stage_use / C::NST;
+        ++stage_use;
+        if (!__all_sync(0xffffffffu, wait_flag(&bar_full[st], round & 1, &s_abort, p.ctrl, p.dev_status))) {
+          ok = false;
+          break;
+        }
+        const uint32_t kbase = stage0 + st * C::STAGE_BYTES;
+        const uint32_t vbase = kbase + C::TILE_BYTES;
+        const int tile_keys = min(BT, item.k1 - (item.k0 + t * BT));
+        const int nvalid = min(16, tile_keys - warp * 16);   // this warp's keys in the tile (may be <= 0)
+        if (nvalid > 0) {
+          // keys past the end: zero their V rows so 0 * (stale or NaN) cannot reach O
+          if (nvalid < 16) {
+            for (int e = lane; e < (16 - nvalid) * (C::ROW_BYTES / 16); e += 32) {
+              const int rr = warp * 16 + nvalid + e / (C::ROW_BYTES / 16);
+              const int bo = (e % (C::ROW_BYTES / 16)) * 16;
+              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sw_addr<C::ATOMS>(vbase, rr, bo)),
+                           "r"(0u)
+                           : "memory");
+            }
+            __syncwarp();
+          }
+          // S^T = K Q^T: rows = the warp's 16 keys, columns = heads; two
+          // accumulators (even / odd 16-dim blocks) halve the dependent chain
+          float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+          const int krow = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+          if constexpr (FP8) {
+            // ldmatrix.x4: (keys 0-7 | 8-15) x (chunk 2j | 2j+1); lane gets bytes 4tig..4tig+3
+#pragma unroll
+            for (int j = 0; j < D / 32; ++j) {
+              uint32_t r[4];
+              ldsm_x4(sw_addr<C::ATOMS>(kbase, krow, (2 * j + (lane >> 4)) * 16), r[0], r[1], r[2], r[3]);
+              const uint32_t a0[4] = {fp8x2_to_h2(r[0] & 0xffffu), fp8x2_to_h2(r[1] & 0xffffu),
+                                      fp8x2_to_h2(r[0] >> 16), fp8x2_to_h2(r[1] >> 16)};
+              const uint32_t a1[4] = {fp8x2_to_h2(r[2] & 0xffffu), fp8x2_to_h2(r[3] & 0xffffu),
+                                      fp8x2_to_h2(r[2] >> 16), fp8x2_to_h2(r[3] >> 16)};
+              mma16816<TM>(sa, a0, qb[2 * j][0], qb[2 * j][1]);
+              mma16816<TM>(sb, a1, qb[2 * j + 1][0], qb[2 * j + 1][1]);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              uint32_t a[4];
+              ldsm_x4(sw_addr<C::ATOMS>(kbase, krow, (kk * 16 + (lane >> 4) * 8) * 2), a[0], a[1], a[2], a[3]);
+              mma16816<TM>((kk & 1) ? sb : sa, a, qb[kk][0], qb[kk][1]);
+            }
+          }
+          // lane: keys grp (s[0..1]) and grp + 8 (s[2..3]), heads 2tig + e
+          float pr[4];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float v0 = grp < nvalid ? (sa[e] + sb[e]) * qk_scale : -INFINITY;
+            const float v1 = grp + 8 < nvalid ? (sa[2 + e] + sb[2 + e]) * qk_scale : -INFINITY;
+            float mx = fmaxf(v0, v1);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float m_new = fmaxf(m_run[e], mx);
+            const float alpha = exp2f(m_run[e] - m_new);
+            m_run[e] = m_new;
+            pr[e] = exp2f(v0 - m_new);
+            pr[2 + e] = exp2f(v1 - m_new);
+            l_part[e] = l_part[e] * alpha + pr[e] + pr[2 + e];
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+              o[i][e] *= alpha;
+              o[i][2 + e] *= alpha;
+            }
+          }
+          // P^T as the B operand: transpose the (keys x heads) fragments in registers
+          const uint32_t pb0 = movm_t(pack2h<TM>(pr[0], pr[1]));   // keys 0-7
+          const uint32_t pb1 = movm_t(pack2h<TM>(pr[2], pr[3]));   // keys 8-15
+          // O^T += V^T P^T
+          if constexpr (FP8) {
+            // ldmatrix.trans of 16-bit units over (keys 0-7 | 8-15) x (16 bytes | next 16):
+            // lane gets dims (2grp, 2grp+1) of keys (2tig, 2tig+1); a byte permute splits
+            // them, so tile 2j+h has rows grp -> dim 32j+16h+2grp, grp+8 -> that + 1
+#pragma unroll
+            for (int j = 0; j < D / 32; ++j) {
+              uint32_t r[4];
+              ldsm_x4_t(sw_addr<C::ATOMS>(vbase, krow, j * 32 + (lane >> 4) * 16), r[0], r[1], r[2], r[3]);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t lo = __byte_perm(r[2 * h], 0u, 0x3120);      // keys 2tig, 2tig+1
+                const uint32_t hi = __byte_perm(r[2 * h + 1], 0u, 0x3120);  // keys 2tig+8, 2tig+9
+                const uint32_t a[4] = {fp8x2_to_h2(lo & 0xffffu), fp8x2_to_h2(lo >> 16), fp8x2_to_h2(hi & 0xffffu),
+                                       fp8x2_to_h2(hi >> 16)};
+                mma16816<TM>(o[2 * j + h], a, pb0, pb1);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+              // matrices: (keys 0-7, dims +0), (keys 0-7, dims +8), (keys 8-15, +0), (keys 8-15, +8)
+              const int vrow = warp * 16 + (lane >> 4) * 8 + (lane & 7);
+              uint32_t a[4];
+              ldsm_x4_t(sw_addr<C::ATOMS>(vbase, vrow, (i * 16 + ((lane >> 3) & 1) * 8) * 2), a[0], a[1], a[2],
+                        a[3]);
+              mma16816<TM>(o[i], a, pb0, pb1);
+            }
+          }
+          if (nvalid < 16) fence_proxy_async_smem();   // our zeroing before the next TMA write
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_empty[st]);
+      }
+      bad = s_bad[slot] != 0;                          // final once the item's last tile landed
+      if (lane == 0) mbar_arrive(&bar_iempty[slot]);   // the item slot may be refilled
+      if (!__all_sync(0xffffffffu, ok)) break;
+      // this warp's state into shared memory
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int h = tig * 2 + e;
+        float l = l_part[e];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        if (h < G) {
+          if (grp == 0) {
+            sMergeML[(warp * G + h) * 2 + 0] = m_run[e];
+            sMergeML[(warp * G + h) * 2 + 1] = l;
+          }
+          float* dst = sMergeO + (warp * G + h) * D;
+#pragma unroll
+          for (int i = 0; i < D / 16; ++i) {
+            if constexpr (FP8) {
+              const int d0 = (i >> 1) * 32 + (i & 1) * 16 + 2 * grp;
+              dst[d0] = o[i][e];
+              dst[d0 + 1] = o[i][2 + e];
+            } else {
+              dst[i * 16 + grp] = o[i][e];
+              dst[i * 16 + grp + 8] = o[i][2 + e];
+            }
+          }
+        }
+      }
+    } else if constexpr (MMA) {
+      // ------------------------------------------------ tensor cores, heads as rows (G = 16)
       // Q (the group's G heads as the 16 rows of the A operand, rows >= G zero)
       uint32_t qa[D / 16][4];
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const int c0 = kk * 16 + tig * 2;
+        // fp8: the contraction index of each 16-dim block is permuted so that
+        // k slots (2tig, 2tig+1 | 2tig+8, 2tig+9) hold dims (4tig, 4tig+1 | 4tig+2, 4tig+3),
+        // the four bytes one ldmatrix lane receives from a key row
+        const int c0 = kk * 16 + (FP8 ? tig * 4 : tig * 2);
+        constexpr int HI_K = FP8 ? 2 : 8;       // offset of the k slots 2tig+8, 2tig+9
         auto ld2 = [&](int row, int col) -> uint32_t {
           if (row >= G) return 0u;
           const uint32_t w = *reinterpret_cast<const uint32_t*>(qg + row * D + col);
@@ -400,8 +590,8 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
         };
         qa[kk][0] = ld2(grp, c0);
         qa[kk][1] = ld2(grp + 8, c0);
-        qa[kk][2] = ld2(grp, c0 + 8);
-        qa[kk][3] = ld2(grp + 8, c0 + 8);
+        qa[kk][2] = ld2(grp, c0 + HI_K);
+        qa[kk][3] = ld2(grp + 8, c0 + HI_K);
       }
       constexpr bool HI = G > 8;                 // rows grp + 8 are real heads
       // an fp8 cache stores K / k_scale: fold the scale into the score scale
@@ -438,26 +628,29 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
             s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+            if constexpr (FP8) {
+              // one ldmatrix.x4 = four 16-byte chunks (64 dims) of the n-tile's 8 keys;
+              // lane (grp, tig) gets bytes 4tig..4tig+3 of key grp in each chunk
 #pragma unroll
-            for (int kk = 0; kk < D / 16; kk += 2) {
-              const int mtx = lane >> 3;
-              const int krow = warp * 16 + nt * 8 + (lane & 7);
-              const int dim = (kk + (mtx >> 1)) * 16 + (mtx & 1) * 8;
-              uint32_t b0, b1, b2, b3;
-              if constexpr (FP8) {
-                // lane (grp, tig) needs bytes 2*tig, 2*tig+1 and +8 of each 16-dim step of key grp
-                const int kr = warp * 16 + nt * 8 + grp;
-                b0 = fp8x2_to_h2(ld_u16(sw_addr<C::ATOMS>(kbase, kr, kk * 16 + tig * 2)));
-                b1 = fp8x2_to_h2(ld_u16(sw_addr<C::ATOMS>(kbase, kr, kk * 16 + tig * 2 + 8)));
-                b2 = fp8x2_to_h2(ld_u16(sw_addr<C::ATOMS>(kbase, kr, kk * 16 + 16 + tig * 2)));
-                b3 = fp8x2_to_h2(ld_u16(sw_addr<C::ATOMS>(kbase, kr, kk * 16 + 16 + tig * 2 + 8)));
-                (void)krow;
-                (void)dim;
-              } else {
-                ldsm_x4(sw_addr<C::ATOMS>(kbase, krow, dim * 2), b0, b1, b2, b3);
+              for (int j = 0; j < D / 64; ++j) {
+                const int krow = warp * 16 + nt * 8 + (lane & 7);
+                uint32_t r[4];
+                ldsm_x4(sw_addr<C::ATOMS>(kbase, krow, (j * 4 + (lane >> 3)) * 16), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                  mma16816<TM>(s[nt], qa[j * 4 + m], fp8x2_to_h2(r[m] & 0xffffu), fp8x2_to_h2(r[m] >> 16));
               }
-              mma16816<TM>(s[nt], qa[kk], b0, b1);
-              mma16816<TM>(s[nt], qa[kk + 1], b2, b3);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < D / 16; kk += 2) {
+                const int mtx = lane >> 3;
+                const int krow = warp * 16 + nt * 8 + (lane & 7);
+                const int dim = (kk + (mtx >> 1)) * 16 + (mtx & 1) * 8;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(sw_addr<C::ATOMS>(kbase, krow, dim * 2), b0, b1, b2, b3);
+                mma16816<TM>(s[nt], qa[kk], b0, b1);
+                mma16816<TM>(s[nt], qa[kk + 1], b2, b3);
+              }
             }
           }
           // online softmax over the warp's keys (rows: head grp, and grp + 8)
@@ -507,26 +700,35 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
           pa[2] = pack2h<TM>(pv[1][0], pv[1][1]);
           pa[3] = pack2h<TM>(pv[1][2], pv[1][3]);
           // O += P V over the warp's 16 keys
+          if constexpr (FP8) {
+            // ldmatrix.trans of 16-bit units: lane (grp, tig) gets, per 8x16-byte
+            // matrix, dims (2grp, 2grp+1) of keys (2tig, 2tig+1). A byte permute
+            // splits them into the even-dim and odd-dim B fragments, so n-tile
+            // 4j+u covers dims 32j + 16(u>>1) + 2n + (u&1) (undone in the epilogue)
 #pragma unroll
-          for (int nd = 0; nd < D / 8; nd += 2) {
-            uint32_t b0, b1, b2, b3;
-            if constexpr (FP8) {
-              // lane (grp, tig) needs dim nd*8+grp of keys 2*tig, 2*tig+1 (b0) and +8 (b1)
-              const int k0 = warp * 16 + tig * 2;
-              auto vb = [&](int key, int dimv) -> uint32_t { return ld_u8(sw_addr<C::ATOMS>(vbase, key, dimv)); };
-              const int d0 = nd * 8 + grp, d1 = d0 + 8;
-              b0 = fp8x2_to_h2(vb(k0, d0) | (vb(k0 + 1, d0) << 8));
-              b1 = fp8x2_to_h2(vb(k0 + 8, d0) | (vb(k0 + 9, d0) << 8));
-              b2 = fp8x2_to_h2(vb(k0, d1) | (vb(k0 + 1, d1) << 8));
-              b3 = fp8x2_to_h2(vb(k0 + 8, d1) | (vb(k0 + 9, d1) << 8));
-            } else {
+            for (int j = 0; j < D / 32; ++j) {
+              const int vrow = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+              uint32_t r[4];
+              ldsm_x4_t(sw_addr<C::ATOMS>(vbase, vrow, j * 32 + (lane >> 4) * 16), r[0], r[1], r[2], r[3]);
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const uint32_t lo = __byte_perm(r[hh * 2], 0u, 0x3120);      // keys 2tig, 2tig+1
+                const uint32_t hi = __byte_perm(r[hh * 2 + 1], 0u, 0x3120);  // keys 2tig+8, 2tig+9
+                mma16816<TM>(o[4 * j + 2 * hh], pa, fp8x2_to_h2(lo & 0xffffu), fp8x2_to_h2(hi & 0xffffu));
+                mma16816<TM>(o[4 * j + 2 * hh + 1], pa, fp8x2_to_h2(lo >> 16), fp8x2_to_h2(hi >> 16));
+              }
+            }
+          } else {
+#pragma unroll
+            for (int nd = 0; nd < D / 8; nd += 2) {
+              uint32_t b0, b1, b2, b3;
               const int mtx = lane >> 3;
               const int vrow = warp * 16 + (mtx & 1) * 8 + (lane & 7);
               const int dim = (nd + (mtx >> 1)) * 8;
               ldsm_x4_t(sw_addr<C::ATOMS>(vbase, vrow, dim * 2), b0, b1, b2, b3);
+              mma16816<TM>(o[nd], pa, b0, b1);
+              mma16816<TM>(o[nd + 1], pa, b2, b3);
             }
-            mma16816<TM>(o[nd], pa, b0, b1);
-            mma16816<TM>(o[nd + 1], pa, b2, b3);
           }
           if (nvalid < 16) fence_proxy_async_smem();   // our zeroing before the next TMA write
         }
@@ -550,9 +752,17 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
           }
 #pragma unroll
           for (int nd = 0; nd < D / 8; ++nd) {
-            float* dst = sMergeO + (warp * G + h) * D + nd * 8 + tig * 2;
-            dst[0] = o[nd][hr * 2];
-            dst[1] = o[nd][hr * 2 + 1];
+            if constexpr (FP8) {
+              // n-tile nd = 4j + u: columns 2tig, 2tig+1 are dims base, base + 2
+              const int j = nd >> 2, u = nd & 3;
+              float* dst = sMergeO + (warp * G + h) * D + j * 32 + (u >> 1) * 16 + tig * 4 + (u & 1);
+              dst[0] = o[nd][hr * 2];
+              dst[2] = o[nd][hr * 2 + 1];
+            } else {
+              float* dst = sMergeO + (warp * G + h) * D + nd * 8 + tig * 2;
+              dst[0] = o[nd][hr * 2];
+              dst[1] = o[nd][hr * 2 + 1];
+            }
           }
         }
       }
@@ -752,6 +962,7 @@ cudaError_t launch_dec(const AttnArgs& a, cudaStream_t s) {
   p.lse = a.lse;
   p.ctrl = (int32_t*)(a.ws + a.lay.ctrl);
   p.item_begin = (const int32_t*)(a.ws + a.lay.row_item_begin);
+  p.row_seq = (const int32_t*)(a.ws + a.lay.row_seq);
   p.part_begin = (const int32_t*)(a.ws + a.lay.row_part_begin);
   p.part_o = (float*)(a.ws + a.lay.part_o);
   p.part_lse = (float*)(a.ws + a.lay.part_lse);
