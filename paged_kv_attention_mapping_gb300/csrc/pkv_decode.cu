@@ -225,6 +225,11 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
   using C = DCfg<TKV, D, G>;
   constexpr bool FP8 = std::is_same<TKV, uint8_t>::value;
   using TM = typename std::conditional<FP8, __half, T>::type;   // mma operand type
+  constexpr bool MMA = C::ELT == 2 || FP8;
+  // keys as the M rows (S^T = K Q^T, O^T = V^T P^T): one n-tile of 8 holds the
+  // whole group when G <= 8, half the MMAs of heads-as-rows. The producer then
+  // also copies each item's q rows (16-bit) into one of two shared slots.
+  constexpr bool KM = MMA && G <= 8;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   unsigned char* sStage = sm;
@@ -232,7 +237,7 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
   float* sMergeO = sQ + G * D;                   // [NCW][G][D]
   float* sMergeML = sMergeO + NCW * G * D;       // [NCW][G][2]
 
-  __shared__ __align__(8) uint64_t bar_full[C::NST], bar_empty[C::NST], bar_ifull[2], bar_iempty[2], bar_cw;
+  __shared__ __align__(8) uint64_t bar_full[C::NST], bar_empty[C::NST], bar_ifull[2], bar_iempty[2], bar_q[2], bar_cw;
   __shared__ Item s_item[2];
   __shared__ int s_bad[2];
   __shared__ volatile int s_abort;
@@ -246,6 +251,7 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_ifull[s], 1);
       mbar_init(&bar_iempty[s], NCW);
+      mbar_init(&bar_q[s], 1);
     }
     mbar_init(&bar_cw, NCW * 32);
     fence_mbar_init();
@@ -262,6 +268,7 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
       tma_prefetch_desc(&mv);
     }
     uint32_t stage_use = 0;
+    uint32_t q_loads = 0;   // q copies issued (lane 0), slots alternate from 0
     for (uint32_t it = 0;; ++it) {
       const int slot = it & 1;
       if (!__all_sync(0xffffffffu, wait_flag(&bar_iempty[slot], ((it >> 1) & 1) ^ 1, &s_abort, p.ctrl,
@@ -296,6 +303,15 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
       if (lane == 0) {
         s_item[slot] = item;
         s_bad[slot] = 0;
+        if constexpr (KM) {
+          if (item.valid) {
+            constexpr uint32_t QB = G * D * 2;
+            mbar_arrive_expect_tx(&bar_q[slot], QB);
+            bulk_load(reinterpret_cast<unsigned char*>(sQ) + slot * QB,
+                      (const T*)p.q + ((int64_t)item.r * p.Hq + item.kvh * G) * D, QB, &bar_q[slot]);
+            ++q_loads;
+          }
+        }
         mbar_arrive(&bar_ifull[slot]);
       }
       if (!item.valid) break;
@@ -368,6 +384,10 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
         const uint32_t uses = stage_use / C::NST + (s < (int)(stage_use % C::NST) ? 1 : 0);
         if (uses > 0) mbar_wait(&bar_full[s], (uses - 1) & 1, 500000000ull);
       }
+      for (int s = 0; s < 2; ++s) {
+        const uint32_t uses = q_loads / 2 + (s < (int)(q_loads % 2) ? 1 : 0);
+        if (uses > 0) mbar_wait(&bar_q[s], (uses - 1) & 1, 500000000ull);
+      }
     }
     return;
   }
@@ -383,10 +403,6 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
     return __all_sync(0xffffffffu, ok);
   };
   const uint32_t stage0 = smem_u32(sStage);
-  constexpr bool MMA = C::ELT == 2 || FP8;
-  // keys as the M rows (S^T = K Q^T, O^T = V^T P^T): one n-tile of 8 holds the
-  // whole group when G <= 8, half the MMAs of heads-as-rows
-  constexpr bool KM = MMA && G <= 8;
   const int grp = lane >> 2, tig = lane & 3;   // mma fragment coordinates
   for (uint32_t it = 0;; ++it) {
     const int slot = it & 1;
@@ -408,6 +424,8 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
       // the contraction index of each 16-dim block is permuted so that k slots
       // (2tig, 2tig+1 | 2tig+8, 2tig+9) hold dims (4tig, 4tig+1 | 4tig+2, 4tig+3),
       // the four bytes one ldmatrix lane receives from a key row.
+      if (!__all_sync(0xffffffffu, wait_flag(&bar_q[slot], (it >> 1) & 1, &s_abort, p.ctrl, p.dev_status))) break;
+      const T* qs = reinterpret_cast<const T*>(reinterpret_cast<const unsigned char*>(sQ) + slot * (G * D * 2));
       uint32_t qb[D / 16][2];
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -417,7 +435,7 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
         for (int u = 0; u < 2; ++u) {
           uint32_t w = 0u;
           if (grp < G) {
-            w = *reinterpret_cast<const uint32_t*>(qg + grp * D + c0 + u * HI_K);
+            w = *reinterpret_cast<const uint32_t*>(qs + grp * D + c0 + u * HI_K);
             if constexpr (FP8 && !std::is_same<T, __half>::value)
               w = pack2h<__half>(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));  // bf16 -> fp16
           }

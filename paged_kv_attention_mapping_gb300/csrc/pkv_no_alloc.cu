@@ -161,7 +161,7 @@ extern "C" int pkv_paged_attention_no_alloc(const void* q, const int32_t* cu_seq
   aa.num_sms = su->num_sms;
   aa.dev_status = status;
   if (tc && launch_prefill_tc(aa, s) != cudaSuccess) return PKV_E_CUDA;
-  if ((decode_supported(aa.dtype, aa.D, aa.P) ? launch_decode(aa, s) : launch_rows(aa, s)) != cudaSuccess)
+  if ((decode_supported(aa.kv_dtype, aa.D, aa.P) ? launch_decode(aa, s) : launch_rows(aa, s)) != cudaSuccess)
     return PKV_E_CUDA;
   if (launch_combine(aa, s) != cudaSuccess) return PKV_E_CUDA;
   return PKV_OK;

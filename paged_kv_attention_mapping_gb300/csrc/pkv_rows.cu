@@ -169,10 +169,14 @@ __global__ void __launch_bounds__(ROWS_WARPS * 32) rows_kernel(AttnArgs a) {
   }
 }
 
-// One warp per (split row, q head).
+// One warp per (split row, q head). The split weights exp(lse_s - lse) are
+// computed one split per lane; the weighted sum then walks the splits with
+// each lane holding D/32 consecutive dims (one vector load per split),
+// unrolled so several splits' loads are in flight at once.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) combine_kernel(AttnArgs a) {
   constexpr int DPL = D / 32;
+  using V = typename std::conditional<DPL == 4, float4, float2>::type;
   const int lane = threadIdx.x & 31;
   const int32_t* ctrl = (const int32_t*)(a.ws + a.lay.ctrl);
   const int32_t* item_begin = (const int32_t*)(a.ws + a.lay.row_item_begin);
@@ -190,25 +194,38 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnArgs a) {
     const int kvh = h / G, hh = h - kvh * G;
     const int nsplit = (item_begin[r + 1] - item_begin[r]) / a.Hkv;
     const int p0 = part_begin[r] + kvh * nsplit;
-    float mx = -INFINITY;
-    for (int s = lane; s < nsplit; s += 32) mx = fmaxf(mx, part_lse[(int64_t)(p0 + s) * G + hh]);
-    mx = warp_max(mx);
-    float sum = 0.f;
-    for (int s = lane; s < nsplit; s += 32) sum += __expf(part_lse[(int64_t)(p0 + s) * G + hh] - mx);
-    sum = warp_sum(sum);
-    const float lse = mx + __logf(sum);
-    float acc[DPL];
+    // lse over the splits: per-lane online max / sum, then one warp reduction
+    float mx = -INFINITY, sm = 0.f;
+    for (int s = lane; s < nsplit; s += 32) {
+      const float v = part_lse[(int64_t)(p0 + s) * G + hh];
+      const float m2 = fmaxf(mx, v);
+      sm = sm * __expf(mx - m2) + __expf(v - m2);
+      mx = m2;
+    }
+    const float gmx = warp_max(mx);
+    sm = mx == -INFINITY ? 0.f : sm * __expf(mx - gmx);
+    const float lse = gmx + __logf(warp_sum(sm));
+    V acc;
+    float* av = reinterpret_cast<float*>(&acc);
 #pragma unroll
-    for (int c = 0; c < DPL; ++c) acc[c] = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const float wgt = __expf(part_lse[(int64_t)(p0 + s) * G + hh] - lse);
-      const float* src = part_o + ((int64_t)(p0 + s) * G + hh) * D + lane * DPL;
+    for (int c = 0; c < DPL; ++c) av[c] = 0.f;
+    for (int s0 = 0; s0 < nsplit; s0 += 32) {
+      const int n = min(32, nsplit - s0);
+      const float wl = lane < n ? __expf(part_lse[(int64_t)(p0 + s0 + lane) * G + hh] - lse) : 0.f;
+      const V* src = reinterpret_cast<const V*>(part_o + ((int64_t)(p0 + s0) * G + hh) * D) + lane;
+      const int64_t stride = (int64_t)G * D / DPL;   // vectors between consecutive splits
+#pragma unroll 4
+      for (int j = 0; j < n; ++j) {
+        const float wgt = __shfl_sync(0xffffffffu, wl, j);
+        const V x = __ldg(src + j * stride);
+        const float* xv = reinterpret_cast<const float*>(&x);
 #pragma unroll
-      for (int c = 0; c < DPL; ++c) acc[c] = fmaf(wgt, src[c], acc[c]);
+        for (int c = 0; c < DPL; ++c) av[c] = fmaf(wgt, xv[c], av[c]);
+      }
     }
     T* dst = (T*)a.out + ((int64_t)r * a.Hq + h) * D + lane * DPL;
 #pragma unroll
-    for (int c = 0; c < DPL; ++c) dst[c] = from_f32<T>(acc[c]);
+    for (int c = 0; c < DPL; ++c) dst[c] = from_f32<T>(av[c]);
     if (a.lse != nullptr && lane == 0) a.lse[(int64_t)r * a.Hq + h] = lse;
   }
 }

@@ -192,6 +192,7 @@ def _fp8_tick(w, dev, qdt, seed=0, poison=True):
     ("bf16", 16, 1, 16, (1, 1, 3, 17, 80), 900), # GQA 16 with chunk rows (causal, row kernel)
     ("bf16", 8, 8, 64, (1, 2, 9), 400),          # no grouping (G = 1)
     ("f16", 16, 8, 32, (1, 33), 520),            # G = 2
+    ("bf16", 32, 8, 64, (1, 1, 5), 9500),        # rows split over several items, combined in the kernel
 ])
 def test_attention_over_fp8_pages(dev, qdt, Hq, Hkv, P, q_lens, max_kv):
     w = W.random_workload(300 + Hq + P, 9, Hq, Hkv, 128, P, qdt, q_lens, max_kv)
