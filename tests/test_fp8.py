@@ -35,6 +35,16 @@ def test_quantize_rounding_and_saturation():
     assert np.array_equal(t[codes], vals.astype(np.float64))   # representable values are fixed points
 
 
+def test_quotient_is_rounded_to_float32_before_the_e4m3_rounding():
+    # x / s is 34.000000353 exactly but 34.0 (the midpoint of 32 and 36) in
+    # float32; ties-to-even then gives 32 (code 0x60). Dividing in float64
+    # would give 36 (0x61).
+    x = np.array([0x42B7F396], dtype=np.uint32).view(np.float32)
+    s = np.array([0x402D217E], dtype=np.uint32).view(np.float32)
+    assert float(np.float64(x[0]) / np.float64(s[0])) > 34.0
+    assert int(F.quantize(x.reshape(1, 1), s)[0, 0]) == 0x60
+
+
 def test_dequantize_scales_per_head():
     codes = np.array([[[0x38, 0x40], [0x38, 0xB8]]], dtype=np.uint8)   # [1, 2 heads, 2]
     v = F.dequantize(codes, np.array([0.5, 3.0]))
@@ -239,3 +249,21 @@ def test_fp8_decode_full_size_sampled(dev):
         ro, rl = oracle.attend_row(qh[r], kseq, vseq, L, w.scale)   # a decode row sees all L keys
         assert np.abs(out[r].float().cpu().numpy() - ro).max() <= TOL_OUT["bf16"]
         assert np.abs(lse[r].cpu().numpy() - rl).max() <= TOL_LSE["bf16"]
+
+
+@pytest.mark.gpu
+def test_append_quant_divides_in_float32(dev):
+    """The float32 quotient case of the codec pin, through the kernel."""
+    H, D = 2, 128
+    x = np.array([0x42B7F396], dtype=np.uint32).view(np.float32)[0]
+    s = np.array([0x402D217E], dtype=np.uint32).view(np.float32)[0]
+    k = np.full((1, H, D), x, dtype=np.float32)
+    scales = np.array([s, s], dtype=np.float32)
+    kc = torch.zeros((1, 16, H, D), dtype=torch.uint8, device=dev)
+    vc = torch.zeros_like(kc)
+    binding.kv_append_quant(torch.from_numpy(k).to(dev), torch.from_numpy(k).to(dev),
+                            torch.zeros(1, dtype=torch.int64, device=dev), kc, vc,
+                            torch.from_numpy(scales).to(dev), torch.from_numpy(scales).to(dev))
+    torch.cuda.synchronize()
+    assert bool((kc[0, 0] == 0x60).all()) and bool((vc[0, 0] == 0x60).all())
+    assert int(kc[0, 1:].sum()) == 0

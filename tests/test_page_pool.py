@@ -119,3 +119,50 @@ def test_shared_prefix_tables_from_requests(lib):
     assert all(pool.refcount(p) == 1 for p in first)
     assert pool.evict(100.0, 1e9, want_free=pool.num_pages) == 16
     assert pool.free_count() == pool.num_pages
+
+
+# ---------------------------------------------------------------------------
+# the reference model itself, pinned to hand-worked sequences (Helios README,
+# "Paged attention": a page is free again when its last holder lets go; Helios
+# blog, "Prefix caching": full blocks only, longest chain reused, sliding TTL,
+# unused leaf blocks evicted first)
+
+def test_model_hand_worked_allocation_and_release():
+    m = PagePoolModel(5, 2)
+    assert m.alloc(2) == [0, 1] and m.alloc(1) == [2]       # lowest free ids first
+    m.retain([1, 1])
+    assert m.ref == [1, 3, 1, 0, 0]
+    m.release([1, 0])
+    assert m.ref == [0, 2, 1, 0, 0] and m.free_count() == 3
+    assert m.alloc(1) == [0]                                 # a freed page is reused
+    with pytest.raises(PoolError):
+        m.release([3])                                       # free page
+    with pytest.raises(PoolError):
+        m.alloc(3)                                           # two pages left
+    assert m.ref == [1, 2, 1, 0, 0]                          # failed calls changed nothing
+
+
+def test_model_hand_worked_prefix_cache_and_eviction():
+    m = PagePoolModel(6, 2)
+    a = m.alloc(3)                                           # [0, 1, 2]
+    assert m.insert([7, 7, 8, 8, 9], a, now=0.0) == 2        # blocks (7,7) and (7,7,8,8); 9 is partial
+    assert m.ref == [2, 2, 1, 0, 0, 0]
+    assert m.lookup([7, 7, 8, 8, 5, 5], now=1.0) == [0, 1]   # longest chain, caller gets a reference
+    assert m.lookup([7, 7, 6, 6], now=2.0) == [0]            # diverges in the second block
+    assert m.lookup([8, 8], now=2.0) == []                   # (8,8) is cached only after (7,7)
+    assert m.ref == [4, 3, 1, 0, 0, 0]
+    m.release(a)
+    m.release([0, 1])
+    m.release([0])
+    assert m.ref == [1, 1, 0, 0, 0, 0]                       # only the cache holds 0 and 1
+    # page 0 has a cached child (page 1), so the leaf 1 goes first, then 0
+    assert m.evict(now=3.0, ttl=100.0, want_free=5) == 1
+    assert m.ref == [1, 0, 0, 0, 0, 0] and m.cache_size() == 1
+    assert m.evict(now=3.0, ttl=100.0, want_free=6) == 1
+    assert m.cache_size() == 0 and m.free_count() == 6
+    # TTL: an entry unused for longer than ttl goes even when no page is wanted
+    b = m.alloc(1)
+    m.insert([1, 2], b, now=10.0)
+    m.release(b)
+    assert m.evict(now=11.0, ttl=5.0) == 0
+    assert m.evict(now=16.5, ttl=5.0) == 1
