@@ -47,23 +47,25 @@ DESCRIPTIONS = {
 }
 
 
-def load_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu record, or None
-    when there is none or the kernel's source changed since the capture."""
+def load_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    record, or None when there is none or the kernel's source changed since."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
-        rec = json.load(f).get(kernel)
-    if not rec:
-        return None
-    src = os.path.join(ROOT, rec["source"])
-    if not os.path.exists(src):
-        return None
-    with open(src, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:12]
-    return int(rec["bytes"]) if h == rec["sha256_12"] else None
+        recs = json.load(f).get("records", [])
+    for rec in recs:
+        if rec["kernel"] != kernel or rec["workload"] != workload:
+            continue
+        src = os.path.join(ROOT, rec["source"])
+        if not os.path.exists(src):
+            return None
+        with open(src, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:12]
+        return int(rec["bytes"]) if h == rec["sha256_12"] else None
+    return None
 
 
 def load_peaks():
@@ -108,7 +110,7 @@ def kernel_roofline(kernel, ktimes, work, peaks, workload):
     device time per launch (CUDA events on the launch stream)."""
     n, total_ms = ktimes[kernel]
     avg_s = total_ms / n / 1000.0
-    traffic = load_traffic(kernel) if workload == "mixed_tick" else None
+    traffic = load_traffic(kernel, workload)
     if kernel == "prefill_tc":
         ach = work["prefill_flops"] / avg_s / 1e12
         return {"kernel": kernel, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
@@ -471,6 +473,7 @@ def main():
 
     peaks = load_peaks()
     work = tick_work(w, kv_elt=1 if args.kv_fp8 else None)
+    tag = args.workload + ("+fp8" if args.kv_fp8 else "") + ("+rope" if args.rope else "")   # traffic record key
     per_kernel = {k: {"launches": n, "avg_us": 1000.0 * t / n, "share": None} for k, (n, t) in ktimes.items()}
     tot = sum(t for _, t in ktimes.values()) or 1.0
     for k, (n, t) in ktimes.items():
@@ -479,10 +482,10 @@ def main():
     roof = None
     if dom is not None:
         avg_s = ktimes[dom][1] / ktimes[dom][0] / 1000.0
-        roof = kernel_roofline(dom, ktimes, work, peaks, args.workload)
-    roof_decode = kernel_roofline("decode", ktimes, work, peaks, args.workload) if "decode" in ktimes else None
+        roof = kernel_roofline(dom, ktimes, work, peaks, tag)
+    roof_decode = kernel_roofline("decode", ktimes, work, peaks, tag) if "decode" in ktimes else None
     app_k = "rope_append" if args.rope else ("kv_append_quant" if args.kv_fp8 else "kv_append")
-    roof_append = kernel_roofline(app_k, ktimes, work, peaks, args.workload) if app_k in ktimes else None
+    roof_append = kernel_roofline(app_k, ktimes, work, peaks, tag) if app_k in ktimes else None
     decode_k = "decode" if "decode" in ktimes else ("rows" if "rows" in ktimes else None)
     decode_gbs = None
     if decode_k and work["decode_bytes"]:
