@@ -241,15 +241,11 @@ static int attention_impl(const void* q, int q_dtype, const int32_t* cu_seqlens_
   pa.Hkv = cache->num_kv_heads;
   pa.max_kv_len = max_kv_len;
   pa.table_cap = max_pages_per_seq * cache->page_size;
-  // Split size depends only on the element size and head_dim (about 1 MB of K+V
-  // per item), never on the other rows of the tick, so a row's result does
-  // not change with the batch it is packed into. It only grows when the
-  // partial results would overflow the workspace.
-  {
-    const int elt = elt_bytes(cache->dtype);
-    int c = (1 << 20) / (2 * cache->head_dim * elt);
-    pa.chunk_min = c < 256 ? 256 : c;
-  }
+  // Split size depends only on the element size and head_dim, never on the
+  // other rows of the tick, so a row's result does not change with the batch
+  // it is packed into. It only grows when the partial results would overflow
+  // the workspace.
+  pa.chunk_min = split_chunk_keys(cache->head_dim, elt_bytes(cache->dtype));
   pa.target_items = 1 << 30;
   pa.tc_min_q = tc ? TC_MIN_Q : 0;
   pa.ws = (char*)workspace;

@@ -243,6 +243,9 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // no item in this call (every CTA reads the same word): leave before any
+  // barrier or tensor-memory set-up
+  if (*(volatile const int32_t*)&p.ctrl[CTRL_N_ITEMS] == 0) return;
   if (tid == 0) {
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(&bar_full[s], 1);

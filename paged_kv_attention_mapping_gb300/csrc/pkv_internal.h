@@ -72,6 +72,17 @@ struct PlanArgs {
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s);
 
+// Keys per split of a row-path (row, KV head): a fixed amount of K+V bytes that
+// depends only on head_dim and the element size, so a row's result never
+// depends on the batch it is packed with. 1 MB at head_dim 128; 128 KB at 64,
+// where ticks of short contexts otherwise leave most SMs idle behind the
+// longest rows (measured on the TinyLlama-shaped decode tick). At least 256.
+inline int32_t split_chunk_keys(int head_dim, int elt) {
+  const int bytes = head_dim >= 128 ? (1 << 20) : (128 << 10);
+  const int c = bytes / (2 * head_dim * elt);
+  return c < 256 ? 256 : c;
+}
+
 // ---------------------------------------------------------------------------
 // kernels' host-side launchers
 

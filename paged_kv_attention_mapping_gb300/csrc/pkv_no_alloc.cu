@@ -123,10 +123,7 @@ extern "C" int pkv_paged_attention_no_alloc(const void* q, const int32_t* cu_seq
   pa.Hkv = c->num_kv_heads;
   pa.max_kv_len = max_kv_len;
   pa.table_cap = max_pages_per_seq * c->page_size;
-  {
-    const int ck = (1 << 20) / (2 * c->head_dim * elt);
-    pa.chunk_min = ck < 256 ? 256 : ck;
-  }
+  pa.chunk_min = split_chunk_keys(c->head_dim, elt);
   pa.target_items = 1 << 30;
   pa.tc_min_q = tc ? kTcMinQ : 0;
   pa.ws = ws;
