@@ -437,15 +437,19 @@ def main():
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
-    meta_bytes = 0
+    # pinned host and device buffers for the tick metadata, allocated once (a
+    # serving loop keeps its staging buffers); pack_tick's output is copied in
+    meta_keys = ("cu_seqlens_q", "kv_lens", "page_tables", "slot_mapping")
+    pk0 = binding.pack_tick(ql, kl, pg, s.page_size, w.num_pages)
+    h_meta = [torch.from_numpy(np.ascontiguousarray(pk0[k])).pin_memory() for k in meta_keys]
+    d_meta = [torch.empty_like(m, device=dev) for m in h_meta]
+    meta_bytes = sum(m.numel() * m.element_size() for m in h_meta)
 
     def e2e_step():
-        nonlocal meta_bytes
         pk = binding.pack_tick(ql, kl, pg, s.page_size, w.num_pages)
-        h_meta = [torch.from_numpy(pk[k]).pin_memory() for k in ("cu_seqlens_q", "kv_lens", "page_tables",
-                                                                  "slot_mapping")]
-        d_meta = [m.to(dev, non_blocking=True) for m in h_meta]
-        meta_bytes = sum(m.numel() * m.element_size() for m in h_meta)
+        for k, hm, dm in zip(meta_keys, h_meta, d_meta):
+            hm.numpy()[...] = pk[k]
+            dm.copy_(hm, non_blocking=True)
         d_q.copy_(h_q, non_blocking=True)
         d_k.copy_(h_k, non_blocking=True)
         d_v.copy_(h_v, non_blocking=True)

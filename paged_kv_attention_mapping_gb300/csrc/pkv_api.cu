@@ -278,6 +278,7 @@ static int attention_impl(const void* q, int q_dtype, const int32_t* cu_seqlens_
   aa.kv_dtype = cache->dtype;
   aa.k_scale = k_scale;
   aa.v_scale = v_scale;
+  aa.after_prefill = tc;
   aa.num_sms = f->num_sms;
   aa.dev_status = f->status;
   if (tc) {

@@ -19,6 +19,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
                                                         int32_t row_vecs, int64_t pool_slots,
                                                         uint4* __restrict__ kc, uint4* __restrict__ vc,
                                                         int32_t* dev_status) {
+  pdl_trigger();   // the attention call's plan does not read what this kernel writes
   const int64_t per_token = 2 * (int64_t)row_vecs;
   const int64_t total = (int64_t)T * per_token;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -69,6 +70,7 @@ __global__ void __launch_bounds__(256) kv_append_quant_kernel(const T* __restric
                                                               const float* __restrict__ v_scale,
                                                               uint4* __restrict__ kc, uint4* __restrict__ vc,
                                                               int32_t* dev_status) {
+  pdl_trigger();   // the attention call's plan does not read what this kernel writes
   const int64_t per_token = 2 * (int64_t)row_vecs;
   const int64_t total = (int64_t)T_ * per_token;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {

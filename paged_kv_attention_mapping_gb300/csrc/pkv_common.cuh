@@ -58,4 +58,11 @@ __device__ __forceinline__ void set_status(int32_t* ctrl_err, int32_t* dev_statu
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
+// Programmatic dependent launch (griddepcontrol). A kernel that calls
+// pdl_trigger() lets the next kernel of its stream, when that one is launched
+// with launch_after_trigger(), start before it finishes; pdl_wait() blocks until
+// the preceding grid has completed and its memory is visible.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 }  // namespace pkv

@@ -244,8 +244,11 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // no item in this call (every CTA reads the same word): leave before any
-  // barrier or tensor-memory set-up
-  if (*(volatile const int32_t*)&p.ctrl[CTRL_N_ITEMS] == 0) return;
+  // barrier set-up
+  if (*(volatile const int32_t*)&p.ctrl[CTRL_N_ITEMS] == 0) {
+    pdl_wait();
+    return;
+  }
   if (tid == 0) {
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(&bar_full[s], 1);
@@ -945,6 +948,9 @@ __global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
       atomicOr(p.dev_status, PKV_DEV_BAD_PAGE);
     }
   }
+  // When launched to overlap the prefill kernel, finish only after it, so that
+  // whatever follows this kernel also follows the prefill.
+  pdl_wait();
 }
 
 template <typename T, typename TKV, int D, int G>
@@ -990,7 +996,17 @@ cudaError_t launch_dec(const AttnArgs& a, cudaStream_t s) {
   p.dev_status = a.dev_status;
   p.k_scale = a.k_scale;
   p.v_scale = a.v_scale;
-  decode_kernel<T, TKV, D, G><<<a.num_sms * CTAS_PER_SM, NTHREADS, C::SMEM, s>>>(mk, mv, p);
+  if (a.after_prefill) {
+    // rows of the decode path and tiles of the prefill kernel are disjoint, and
+    // the plan both read finished before the prefill kernel started: this grid
+    // may start as soon as the prefill kernel has (its CTAs fill SMs that the
+    // prefill kernel's tail leaves idle)
+    const cudaError_t e = launch_after_trigger(decode_kernel<T, TKV, D, G>, dim3(a.num_sms * CTAS_PER_SM),
+                                               dim3(NTHREADS), C::SMEM, s, mk, mv, p);
+    if (e != cudaSuccess) return e;
+  } else {
+    decode_kernel<T, TKV, D, G><<<a.num_sms * CTAS_PER_SM, NTHREADS, C::SMEM, s>>>(mk, mv, p);
+  }
   return cudaGetLastError();
 }
 

@@ -72,6 +72,24 @@ struct PlanArgs {
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s);
 
+// Launch with programmatic stream serialization: the kernel may start as soon
+// as the preceding kernel of the stream calls pdl_trigger() (or completes).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after_trigger(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                 Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Keys per split of a row-path (row, KV head): a fixed amount of K+V bytes that
 // depends only on head_dim and the element size, so a row's result never
 // depends on the batch it is packed with. 1 MB at head_dim 128; 128 KB at 64,
@@ -105,6 +123,7 @@ struct AttnArgs {
   int kv_dtype = -1;               // cache element type (the q type unless an fp8 cache)
   const float* k_scale = nullptr;  // fp8 caches: per-KV-head scales (device)
   const float* v_scale = nullptr;
+  bool after_prefill = false;      // the prefill kernel was launched just before (decode may overlap it)
 };
 
 cudaError_t launch_append(const void* k, const void* v, const int64_t* slots, int32_t T, void* kc, void* vc,

@@ -155,6 +155,7 @@ extern "C" int pkv_paged_attention_no_alloc(const void* q, const int32_t* cu_seq
   aa.lay = lay;
   aa.dtype = c->dtype;
   aa.kv_dtype = c->dtype;
+  aa.after_prefill = tc;
   aa.num_sms = su->num_sms;
   aa.dev_status = status;
   if (tc && launch_prefill_tc(aa, s) != cudaSuccess) return PKV_E_CUDA;

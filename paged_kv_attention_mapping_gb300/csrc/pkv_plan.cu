@@ -333,6 +333,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
     ctrl[CTRL_N_PARTIALS] = carry_parts;
     if (s_err) atomicOr(dev_status, s_err);
   }
+  // This kernel may have started while the preceding kernel (the append) still
+  // ran; finishing only after it makes every later launch see the appended K/V.
+  pdl_wait();
 }
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
@@ -341,7 +344,9 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
   if (attr != cudaSuccess) return attr;
   const size_t smem = a.B <= PLAN_SMEM_SEQS ? (size_t)(3 * a.B + 2) * 4 : 0;
   KernelTimer timer("plan", s);
-  plan_kernel<<<1, 1024, smem, s>>>(a, a.dev_status);
+  // may overlap the preceding append, which it does not read (see pdl_wait above)
+  cudaError_t e = launch_after_trigger(plan_kernel, dim3(1), dim3(1024), smem, s, a, a.dev_status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

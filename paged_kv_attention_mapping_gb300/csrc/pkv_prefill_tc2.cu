@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __shared__ int s_bad;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();   // the decode kernel that follows reads nothing this kernel writes
   // no tile in this call (every CTA reads the same word): leave before any
   // barrier or tensor-memory set-up
   if (*(volatile const int32_t*)&p.ctrl[CTRL_N_TILES] == 0) return;

@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(256) rope_append_kernel(const T* __restrict__ 
                                                           int32_t Hq, int32_t Hkv, int32_t D, int64_t pool_slots,
                                                           T* __restrict__ kc, T* __restrict__ vc, T* __restrict__ q_out,
                                                           int32_t* dev_status) {
+  pdl_trigger();   // the attention call's plan does not read what this kernel writes
   constexpr int E = 16 / sizeof(T);
   const int half = D / 2;
   const int rv = half / E;                       // rotation vectors per Q/K row
