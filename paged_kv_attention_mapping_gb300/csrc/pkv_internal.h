@@ -90,16 +90,12 @@ cudaError_t launch_after_trigger(void (*kernel)(KArgs...), dim3 grid, dim3 block
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
-// Keys per split of a row-path (row, KV head): a fixed amount of K+V bytes that
-// depends only on head_dim and the element size, so a row's result never
-// depends on the batch it is packed with. 1 MB at head_dim 128; 128 KB at 64,
-// where ticks of short contexts otherwise leave most SMs idle behind the
-// longest rows (measured on the TinyLlama-shaped decode tick). At least 256.
-inline int32_t split_chunk_keys(int head_dim, int elt) {
-  const int bytes = head_dim >= 128 ? (1 << 20) : (128 << 10);
-  const int c = bytes / (2 * head_dim * elt);
-  return c < 256 ? 256 : c;
-}
+// Keys per split of a row-path (row, KV head). It depends only on head_dim,
+// so a row's result never depends on the batch it is packed with: 2048 keys at
+// head_dim 128 (1 MB of bf16 K+V, 512 KB of fp8) and 512 at 64, where ticks of
+// short contexts otherwise leave most SMs idle behind the longest rows
+// (measured on the TinyLlama- and Qwen3-shaped decode ticks, 16-bit and fp8).
+inline int32_t split_chunk_keys(int head_dim, int /*elt*/) { return head_dim >= 128 ? 2048 : 512; }
 
 // ---------------------------------------------------------------------------
 // kernels' host-side launchers

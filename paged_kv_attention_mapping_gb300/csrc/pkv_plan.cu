@@ -184,10 +184,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
 
   // pass 1: check every sequence; count the keys the row path will visit
   unsigned long long my_keys = 0;
-  int my_err = 0;
+  int my_err = 0, my_tc = 0;
   for (int b = tid; b < a.B; b += blockDim.x) {
     const SeqInfo s = seq_info(a, b);
     if (s.bad) my_err = PKV_DEV_BAD_LENGTHS;
+    my_tc |= s.tc ? 1 : 0;
     if (!s.bad && !s.tc && s.q > 0)
       my_keys += (unsigned long long)s.q * (unsigned long long)(s.L - s.q) +
                  (unsigned long long)s.q * (s.q + 1) / 2;
@@ -203,6 +204,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
   }
   __syncthreads();
 
+  const bool any_tc = __syncthreads_or(my_tc) != 0;   // no prefill-kernel sequence: skip pass 3
   // split size: about target_items items, at least chunk_min keys, multiple of 64
   const long long work = (long long)s_keys * a.Hkv;
   long long C = (work + a.target_items - 1) / a.target_items;
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
 
   // pass 3: (sequence, q tile) pairs of the prefill kernel, longest first
   int carry_pairs = 0;
-  for (int base = 0; base < a.B; base += blockDim.x) {
+  for (int base = 0; any_tc && base < a.B; base += blockDim.x) {
     const int b = base + tid;
     int n = 0;
     if (b < a.B) {
@@ -278,49 +280,51 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
   if (tid == 0) pair_begin[a.B] = carry_pairs;
   __syncthreads();
   const int n_pairs = carry_pairs;
-  for (int i = tid; i < HIST; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
-  auto pair_work = [&](int p, int* b_out, int* qt_out) {
-    const int b = upper_bound_written(pair_begin, a.B + 1, p) - 1;   // shared memory when B fits
-    const int qt = p - pair_begin[b];
-    const SeqInfo s = seq_info(a, b);
-    const int q1 = min(s.q, (qt + 1) * TC_BM);
-    const int keys = s.L - s.q + q1;  // keys the tile's last row sees
-    int w = (keys + TC_BN - 1) / TC_BN;
-    *b_out = b;
-    *qt_out = qt;
-    return min(w, HIST - 1);
-  };
-  for (int p = tid; p < n_pairs; p += blockDim.x) {
-    int b, qt;
-    atomicAdd(&hist[pair_work(p, &b, &qt)], 1);
-  }
-  __syncthreads();
-  // descending exclusive offsets: hist[w] <- number of pairs with work > w
-  {
-    constexpr int PER = HIST / 1024;
-    int vals[PER], sum = 0;
-#pragma unroll
-    for (int k = 0; k < PER; ++k) {
-      vals[k] = hist[HIST - 1 - (tid * PER + k)];
-      sum += vals[k];
+  if (n_pairs > 0) {   // block-uniform
+    for (int i = tid; i < HIST; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    auto pair_work = [&](int p, int* b_out, int* qt_out) {
+      const int b = upper_bound_written(pair_begin, a.B + 1, p) - 1;   // shared memory when B fits
+      const int qt = p - pair_begin[b];
+      const SeqInfo s = seq_info(a, b);
+      const int q1 = min(s.q, (qt + 1) * TC_BM);
+      const int keys = s.L - s.q + q1;  // keys the tile's last row sees
+      int w = (keys + TC_BN - 1) / TC_BN;
+      *b_out = b;
+      *qt_out = qt;
+      return min(w, HIST - 1);
+    };
+    for (int p = tid; p < n_pairs; p += blockDim.x) {
+      int b, qt;
+      atomicAdd(&hist[pair_work(p, &b, &qt)], 1);
     }
-    int t;
-    int run = block_scan_excl(sum, &t, sm);
-#pragma unroll
-    for (int k = 0; k < PER; ++k) {
-      hist[HIST - 1 - (tid * PER + k)] = run;
-      run += vals[k];
+    __syncthreads();
+    // descending exclusive offsets: hist[w] <- number of pairs with work > w
+    {
+      constexpr int PER = HIST / 1024;
+      int vals[PER], sum = 0;
+  #pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        vals[k] = hist[HIST - 1 - (tid * PER + k)];
+        sum += vals[k];
+      }
+      int t;
+      int run = block_scan_excl(sum, &t, sm);
+  #pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        hist[HIST - 1 - (tid * PER + k)] = run;
+        run += vals[k];
+      }
     }
+    __syncthreads();
+    for (int p = tid; p < n_pairs; p += blockDim.x) {
+      int b, qt;
+      const int w = pair_work(p, &b, &qt);
+      const int pos = atomicAdd(&hist[w], 1);
+      pairs[pos] = make_int2(b, qt);
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  for (int p = tid; p < n_pairs; p += blockDim.x) {
-    int b, qt;
-    const int w = pair_work(p, &b, &qt);
-    const int pos = atomicAdd(&hist[w], 1);
-    pairs[pos] = make_int2(b, qt);
-  }
-  __syncthreads();
   if (tid == 0) {
     ctrl[CTRL_ERR] = s_err;
     ctrl[CTRL_N_ITEMS] = carry_items;
