@@ -38,7 +38,9 @@ namespace {
 constexpr int BT = 64;             // keys per tile
 constexpr int NCW = 4;             // compute warps
 constexpr int NTHREADS = (NCW + 1) * 32;
-constexpr int CTAS_PER_SM = 2;
+#ifndef PKV_DEC_CPS_SMALL
+#define PKV_DEC_CPS_SMALL 3
+#endif
 
 struct DecParams {
   const int32_t* cu;
@@ -201,9 +203,15 @@ struct DCfg {
   static constexpr int MERGE_BYTES = NCW * G * D * 4 + NCW * G * 8;
   // Stages: enough bytes in flight to cover HBM latency. Small stages (fp8,
   // head_dim 64) get as many as fit two CTAs per SM, up to 6.
+  // CTAs per SM: small stages (head_dim 64 at 16 bits, fp8) run CPS_SMALL CTAs
+  // so that more producers stream at once (a CTA's TMA boxes are processed in
+  // order, so each CTA's stream has a fixed rate); the rest run 2.
+  static constexpr int CPS = (STAGE_BYTES <= 16384 && ELT <= 2 && G <= 8) ? PKV_DEC_CPS_SMALL : 2;
   static constexpr int BASE_NST = STAGE_BYTES <= 32768 ? 3 : 2;
-  static constexpr int FIT_NST = (112 * 1024 - Q_BYTES - MERGE_BYTES - 1024) / STAGE_BYTES;
-  static constexpr int NST = FIT_NST > BASE_NST ? (FIT_NST < 6 ? FIT_NST : 6) : BASE_NST;
+  // 228 KB of shared memory per SM, 1 KB of it reserved per CTA, ~0.5 KB static
+  static constexpr int FIT_NST = (233472 / CPS - 1536 - Q_BYTES - MERGE_BYTES - 1024) / STAGE_BYTES;
+  static constexpr int NST = CPS > 2 ? (FIT_NST < 6 ? FIT_NST : 6)
+                                     : (FIT_NST > BASE_NST ? (FIT_NST < 6 ? FIT_NST : 6) : BASE_NST);
   static constexpr int SMEM = NST * STAGE_BYTES + Q_BYTES + MERGE_BYTES + 1024;
   static constexpr int DPL = D / 32;                   // PV: dims per lane
   static_assert(ROW_BYTES % 128 == 0, "key rows must be whole swizzle atoms");
@@ -220,7 +228,7 @@ __device__ __forceinline__ uint32_t sw_addr(uint32_t tile_base, int row, int byt
 // T: query/output element type; TKV: cache element type (T, or uint8_t for an
 // fp8 e4m3 cache, dequantised to fp16 in registers for the mma.sync path).
 template <typename T, typename TKV, int D, int G>
-__global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
+__global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
     decode_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv, DecParams p) {
   using C = DCfg<TKV, D, G>;
   constexpr bool FP8 = std::is_same<TKV, uint8_t>::value;
@@ -1001,11 +1009,11 @@ cudaError_t launch_dec(const AttnArgs& a, cudaStream_t s) {
     // the plan both read finished before the prefill kernel started: this grid
     // may start as soon as the prefill kernel has (its CTAs fill SMs that the
     // prefill kernel's tail leaves idle)
-    const cudaError_t e = launch_after_trigger(decode_kernel<T, TKV, D, G>, dim3(a.num_sms * CTAS_PER_SM),
+    const cudaError_t e = launch_after_trigger(decode_kernel<T, TKV, D, G>, dim3(a.num_sms * C::CPS),
                                                dim3(NTHREADS), C::SMEM, s, mk, mv, p);
     if (e != cudaSuccess) return e;
   } else {
-    decode_kernel<T, TKV, D, G><<<a.num_sms * CTAS_PER_SM, NTHREADS, C::SMEM, s>>>(mk, mv, p);
+    decode_kernel<T, TKV, D, G><<<a.num_sms * C::CPS, NTHREADS, C::SMEM, s>>>(mk, mv, p);
   }
   return cudaGetLastError();
 }
