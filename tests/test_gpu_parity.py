@@ -114,6 +114,9 @@ RAGGED = [
     (8, 7, 16, 16, 64, 16, "f32", (1,), 300),
     (9, 3, 8, 8, 128, 256, "bf16", (130, 1), 400),      # g = 1: single-query-tile prefill kernel
     (10, 4, 16, 4, 64, 32, "f16", (200, 1, 70), 600),   # page 32 < tile: several pages per TMA tile
+    (13, 3, 32, 2, 128, 256, "bf16", (130, 1), 500),    # g = 16: eight head pairs per KV head in the prefill kernel
+    (14, 3, 8, 4, 64, 64, "f16", (150, 1), 400),        # g = 2, page 64: one page per decode tile
+    (15, 3, 16, 8, 128, 128, "bf16", (140, 1), 600),    # page 128 = one prefill KV tile per page
 ]
 
 
@@ -139,6 +142,61 @@ def test_idle_sequences_and_empty_tick(dev):
     binding.paged_attention(q, torch.tensor([0, 0], dtype=torch.int32, device=dev),
                             torch.tensor([5], dtype=torch.int32, device=dev),
                             torch.zeros((1, 1), dtype=torch.int32, device=dev), kc, kc, 0.125, 16, workspace=ws)
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f16", 64), ("f32", 64)])
+def test_one_key_context_returns_v(dev, dtype, d):
+    """A context of one key (the token just appended): out is that token's V
+    exactly, lse is scale * q.k (the softmax of one score is 1)."""
+    B, Hq, Hkv, P = 5, 16, 4, 16
+    rng = np.random.default_rng(21)
+    q = W.round_to_dtype(rng.standard_normal((B, Hq, d), dtype=np.float32), dtype)
+    k = W.round_to_dtype(rng.standard_normal((B, Hkv, d), dtype=np.float32), dtype)
+    v = W.round_to_dtype(rng.standard_normal((B, Hkv, d), dtype=np.float32), dtype)
+    pages = [[b] for b in range(B)]
+    packed = binding.pack_tick([1] * B, [1] * B, pages, P, B)
+    kc = torch.full((B, P, Hkv, d), float("nan"), dtype=W.torch_dtype(dtype), device=dev)
+    vc = kc.clone()
+    scale = 1.0 / np.sqrt(d)
+    binding.kv_append(to_dev(k, dtype, dev), to_dev(v, dtype, dev), idx_dev(packed["slot_mapping"], dev), kc, vc)
+    out, lse = binding.paged_attention(to_dev(q, dtype, dev), idx_dev(packed["cu_seqlens_q"], dev),
+                                       idx_dev(packed["kv_lens"], dev), idx_dev(packed["page_tables"], dev), kc,
+                                       vc, scale, 1)
+    torch.cuda.synchronize()
+    g = Hq // Hkv
+    want = np.repeat(np.asarray(v, np.float32), g, axis=1)        # q head h reads KV head h // g
+    assert np.array_equal(to_host(out).astype(np.float32), want)
+    qk = np.einsum("bhd,bhd->bh", np.asarray(q, np.float64), np.repeat(np.asarray(k, np.float64), g, axis=1))
+    assert np.abs(lse.cpu().numpy() - scale * qk).max() <= TOL_LSE[dtype]
+
+
+def test_back_to_back_ticks_without_sync(dev):
+    """Two ticks (chunks and decode rows) issued one after the other on one
+    stream with no host synchronisation, then the first again into the same
+    buffers: both match the oracle and the repeat is bit-identical."""
+    ws_ = []
+    res = []
+    for seed in (31, 32):
+        w = W.random_workload(seed, 6, 16, 4, 128, 256, "bf16", (1, 1, 150), 900)
+        vals = W.host_values(w)
+        ql, kl, pg = lists(w)
+        packed = binding.pack_tick(ql, kl, pg, w.shape.page_size, w.num_pages)
+        kc, vc = to_dev(vals.k_cache, "bf16", dev), to_dev(vals.v_cache, "bf16", dev)
+        args = (to_dev(vals.q, "bf16", dev), idx_dev(packed["cu_seqlens_q"], dev), idx_dev(packed["kv_lens"], dev),
+                idx_dev(packed["page_tables"], dev), kc, vc, w.scale, w.max_kv_len)
+        ws_.append((w, vals, packed, args, to_dev(vals.k_new, "bf16", dev), to_dev(vals.v_new, "bf16", dev)))
+    for w, vals, packed, args, kn, vn in ws_:
+        binding.kv_append(kn, vn, idx_dev(packed["slot_mapping"], dev), args[4], args[5])
+        res.append(binding.paged_attention(*args))
+    w, vals, packed, args, kn, vn = ws_[0]
+    again = binding.paged_attention(*args)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    for (w, vals, packed, args, kn, vn), (out, lse) in zip(ws_, res):
+        ro, rl = oracle_tick(w, vals.q, vals.k_new, vals.v_new, vals.k_cache, vals.v_cache)
+        assert np.abs(to_host(out).astype(np.float64) - ro).max() <= TOL_OUT["bf16"]
+        assert np.abs(lse.cpu().numpy() - rl).max() <= TOL_LSE["bf16"]
+    assert torch.equal(again[0], res[0][0]) and torch.equal(again[1], res[0][1])
 
 
 def test_packing_does_not_change_a_row(dev):
