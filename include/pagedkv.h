@@ -72,9 +72,11 @@ typedef enum {
 
 /* Bits of the device status word. */
 #define PKV_DEV_BAD_SLOT 0x1    /* kv_append: slot >= num_pages * page_size; that row skipped */
-#define PKV_DEV_BAD_LENGTHS 0x2 /* attention: q_len < 0, kv_len < q_len, kv_len < 1 with rows,
-                                   kv_len > max_kv_len or > max_pages_per_seq * page_size;
-                                   that sequence's rows are skipped */
+#define PKV_DEV_BAD_LENGTHS 0x2 /* attention: kv_len < q_len, kv_len < 1 with rows,
+                                   kv_len > max_kv_len or > max_pages_per_seq * page_size:
+                                   that sequence's rows are skipped; cu_seqlens_q not
+                                   non-decreasing from 0 to total_q (some q_len < 0):
+                                   every row of the call is skipped */
 #define PKV_DEV_BAD_PAGE 0x4    /* attention: a page id needed by a row is outside the pool;
                                    that row's output is left unwritten */
 #define PKV_DEV_TIMEOUT 0x8     /* a kernel's internal wait gave up (a bug, never expected);

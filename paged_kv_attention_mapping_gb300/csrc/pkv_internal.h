@@ -43,7 +43,7 @@ enum Ctrl : int {
 };
 
 struct PlanLayout {
-  size_t ctrl, row_seq, row_item_begin, row_part_begin, split_rows, seq_pair_begin, tc_pairs,
+  size_t ctrl, row_seq, row_item_begin, row_part_begin, split_rows, seq_pair_begin, seq_offs, tc_pairs,
       part_lse, part_o, total;
   int32_t partial_cap;  // partial results the workspace can hold
   int32_t pair_cap;     // (seq, q tile) pairs the workspace can hold

@@ -29,6 +29,7 @@ PlanLayout plan_layout(int32_t B, int32_t T, int32_t Hq, int32_t Hkv, int32_t D,
   L.row_part_begin = off;  off += align256((size_t)T * 4 + 4);
   L.split_rows = off;      off += align256((size_t)T * 4 + 4);
   L.seq_pair_begin = off;  off += align256(((size_t)B + 1) * 4);
+  L.seq_offs = off;        off += align256((size_t)3 * B * 4 + 4);
   L.pair_cap = T / TC_BM + B + 1;
   L.tc_pairs = off;        off += align256((size_t)L.pair_cap * 8);
   const int g = Hq / Hkv;
@@ -132,28 +133,39 @@ __device__ void block_scan3(const int (&v)[3], int (&ex)[3], int (&tot)[3], int 
 constexpr int HIST = 2048;
 
 struct SeqInfo {
-  int q, L;
+  int c0, q, L;
   bool bad, tc;
 };
 
-__device__ __forceinline__ SeqInfo seq_info(const PlanArgs& a, int b) {
+// `partition_bad`: cu_seqlens_q does not cut [0, T) into consecutive ranges,
+// so no row can be given to a sequence and every sequence counts as bad.
+__device__ __forceinline__ SeqInfo seq_info(const PlanArgs& a, int b, bool partition_bad) {
   SeqInfo s;
-  const int c0 = a.cu[b], c1 = a.cu[b + 1];
-  s.q = c1 - c0;
+  s.c0 = a.cu[b];
+  const int c1 = a.cu[b + 1];
+  s.q = c1 - s.c0;
   s.L = a.kv_lens[b];
-  s.bad = s.q < 0 || c0 < 0 || c1 > a.T ||
+  s.bad = partition_bad || s.q < 0 || s.c0 < 0 || c1 > a.T ||
           (s.q > 0 && (s.L < s.q || s.L > a.max_kv_len || s.L > a.table_cap));
   s.tc = !s.bad && a.tc_min_q > 0 && s.q >= a.tc_min_q;
   return s;
 }
 
-constexpr int PLAN_SMEM_SEQS = 12000;   // sequences whose lengths are staged in shared memory
+// Sum of ceil(k / C) over k = 1 .. K (K >= 0): with K = m C + r, the first m C
+// terms give C (1 + .. + m) and the last r terms m + 1 each.
+__device__ __forceinline__ long long ceil_div_prefix(unsigned K, unsigned C) {
+  const unsigned m = K / C, r = K - m * C;
+  return (long long)C * m * (m + 1) / 2 + (long long)r * (m + 1);
+}
+
+constexpr int PLAN_SMEM_SEQS = 8192;   // sequences whose lengths and offsets are staged in shared memory
 
 __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_status) {
   // stage cu_seqlens_q and kv_lens in shared memory: every row below searches them
   extern __shared__ int32_t s_seq[];
   PlanArgs a = a_in;
-  if (a_in.B <= PLAN_SMEM_SEQS) {
+  const bool staged = a_in.B <= PLAN_SMEM_SEQS;
+  if (staged) {
     for (int i = threadIdx.x; i <= a_in.B; i += blockDim.x) s_seq[i] = __ldg(a_in.cu + i);
     for (int i = threadIdx.x; i < a_in.B; i += blockDim.x) s_seq[a_in.B + 1 + i] = __ldg(a_in.kv_lens + i);
     a.cu = s_seq;
@@ -166,7 +178,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
   int32_t* part_begin = (int32_t*)(a.ws + a.lay.row_part_begin);
   int32_t* split_rows = (int32_t*)(a.ws + a.lay.split_rows);
   int32_t* pair_begin_g = (int32_t*)(a.ws + a.lay.seq_pair_begin);
-  int32_t* pair_begin = a_in.B <= PLAN_SMEM_SEQS ? s_seq + 2 * a_in.B + 1 : pair_begin_g;
+  int32_t* pair_begin = staged ? s_seq + 2 * a_in.B + 1 : pair_begin_g;
+  // per sequence: first item, first partial slot, first split-row index
+  volatile int32_t* seq_off = staged ? s_seq + 3 * a_in.B + 2 : (int32_t*)(a.ws + a.lay.seq_offs);
   int2* pairs = (int2*)(a.ws + a.lay.tc_pairs);
 
   __shared__ unsigned long long s_keys;
@@ -175,18 +189,22 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
   __shared__ int sm3[3][32];
   __shared__ int hist[HIST];
   const int tid = threadIdx.x;
-  if (tid == 0) {
-    s_keys = 0;
-    s_err = 0;
-    if (a.cu[0] != 0 || a.cu[a.B] != a.T) s_err = PKV_DEV_BAD_LENGTHS;
-  }
-  __syncthreads();
+  const int B = a.B, Hkv = a.Hkv;
 
   // pass 1: check every sequence; count the keys the row path will visit
+  const bool ends_bad = a.cu[0] != 0 || a.cu[B] != a.T;
+  int my_desc = 0;
+  for (int b = tid; b < B; b += blockDim.x) my_desc |= a.cu[b + 1] < a.cu[b] ? 1 : 0;
+  const bool partition_bad = __syncthreads_or(my_desc) != 0 || ends_bad;
+  if (tid == 0) {
+    s_keys = 0;
+    s_err = partition_bad ? PKV_DEV_BAD_LENGTHS : 0;
+  }
+  __syncthreads();
   unsigned long long my_keys = 0;
   int my_err = 0, my_tc = 0;
-  for (int b = tid; b < a.B; b += blockDim.x) {
-    const SeqInfo s = seq_info(a, b);
+  for (int b = tid; b < B; b += blockDim.x) {
+    const SeqInfo s = seq_info(a, b, partition_bad);
     if (s.bad) my_err = PKV_DEV_BAD_LENGTHS;
     my_tc |= s.tc ? 1 : 0;
     if (!s.bad && !s.tc && s.q > 0)
@@ -202,65 +220,81 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
     atomicAdd(&s_keys, my_keys);
     if (my_err) atomicOr(&s_err, my_err);
   }
-  __syncthreads();
-
   const bool any_tc = __syncthreads_or(my_tc) != 0;   // no prefill-kernel sequence: skip pass 3
   // split size: about target_items items, at least chunk_min keys, multiple of 64
-  const long long work = (long long)s_keys * a.Hkv;
+  const long long work = (long long)s_keys * Hkv;
   long long C = (work + a.target_items - 1) / a.target_items;
   if (C < a.chunk_min) C = a.chunk_min;
   C = (C + 63) / 64 * 64;
   const long long c_max = ((long long)a.max_kv_len + 63) / 64 * 64;
-  if (C > c_max) C = c_max < 64 ? 64 : c_max;
+  if (C > c_max) C = c_max;
+  if (C < 64) C = 64;
 
-  // Each thread owns a contiguous run of rows and walks the sequence
-  // boundaries along it; one 3-value block scan turns the per-thread counts
-  // (items, partial slots, split rows) into offsets.
-  const int R = (a.T + blockDim.x - 1) / blockDim.x;
-  const int r_begin = min(a.T, tid * R), r_end = min(a.T, r_begin + R);
-  auto for_rows = [&](auto&& f) {
-    if (r_begin >= r_end) return;
-    int b = upper_bound_i32(a.cu, a.B + 1, r_begin) - 1;
-    for (int r = r_begin; r < r_end; ++r) {
-      while (b + 1 < a.B && a.cu[b + 1] <= r) ++b;
-      int n = 0, bb = -1;
-      if (b >= 0 && b < a.B) {
-        const SeqInfo si = seq_info(a, b);
-        const int c0 = a.cu[b];
-        if (!si.bad && !si.tc && r >= c0 && r < c0 + si.q) {
-          bb = b;
-          n = (int)((si.L - si.q + (r - c0) + 1 + C - 1) / C);
+  // pass 2a: per sequence, in closed form, the items (row, KV head, split),
+  // partial slots and split rows of its rows, turned into offsets by a block
+  // scan. Row i of a row-path sequence sees k = L - q + 1 + i keys and makes
+  // ceil(k / C) items per KV head; it is split when k > C.
+  int carry[3];
+  for (int guard = 0; guard < 40; ++guard) {
+    carry[0] = carry[1] = carry[2] = 0;
+    const unsigned Cu = (unsigned)C;
+    for (int base = 0; base < B; base += blockDim.x) {
+      const int b = base + tid;
+      int cnt[3] = {0, 0, 0}, ex[3], tot[3];
+      if (b < B) {
+        const SeqInfo s = seq_info(a, b, partition_bad);
+        if (!s.bad && !s.tc && s.q > 0) {
+          const unsigned k_lo = (unsigned)(s.L - s.q + 1), k_hi = (unsigned)s.L;
+          const long long f_hi = ceil_div_prefix(k_hi, Cu);
+          cnt[0] = (int)(f_hi - ceil_div_prefix(k_lo - 1, Cu)) * Hkv;
+          const unsigned k_s = k_lo > Cu + 1 ? k_lo : Cu + 1;   // first split row's key count
+          if (k_hi >= k_s) {
+            cnt[1] = (int)(f_hi - ceil_div_prefix(k_s - 1, Cu)) * Hkv;
+            cnt[2] = (int)(k_hi - k_s + 1);
+          }
         }
       }
-      f(r, n, bb);
-    }
-  };
-  int ex[3], tot[3];
-  for (int guard = 0; guard < 40; ++guard) {
-    int cnt[3] = {0, 0, 0};
-    for_rows([&](int, int n, int) {
-      cnt[0] += n * a.Hkv;
-      if (n > 1) {
-        cnt[1] += n * a.Hkv;
-        cnt[2] += 1;
+      block_scan3(cnt, ex, tot, sm3);
+      if (b < B) {
+        seq_off[3 * b + 0] = carry[0] + ex[0];
+        seq_off[3 * b + 1] = carry[1] + ex[1];
+        seq_off[3 * b + 2] = carry[2] + ex[2];
       }
-    });
-    block_scan3(cnt, ex, tot, sm3);
-    if (tot[1] <= a.lay.partial_cap || C >= c_max) break;
+#pragma unroll
+      for (int k = 0; k < 3; ++k) carry[k] += tot[k];
+    }
+    if (carry[1] <= a.lay.partial_cap || C >= c_max) break;
     C = C * 2 < c_max ? C * 2 : c_max;   // grow the split until the partials fit
   }
+  __syncthreads();   // seq_off complete
+
+  // pass 2b: per row (consecutive rows on consecutive threads), its sequence
+  // by binary search and its item / partial offsets from the same closed form
   {
-    int it = ex[0], pt = ex[1], sp = ex[2];
-    for_rows([&](int r, int n, int bb) {
+    const unsigned Cu = (unsigned)C;
+    for (int r = tid; r < a.T; r += blockDim.x) {
+      int bb = -1, it = 0, pt = -1;
+      if (!partition_bad) {
+        const int b = upper_bound_i32(a.cu, B + 1, r) - 1;   // cu[b] <= r < cu[b + 1]
+        const SeqInfo s = seq_info(a, b, false);
+        it = seq_off[3 * b];
+        if (!s.bad && !s.tc) {
+          bb = b;
+          const unsigned k_lo = (unsigned)(s.L - s.q + 1), k = k_lo + (unsigned)(r - s.c0);
+          it += (int)(ceil_div_prefix(k - 1, Cu) - ceil_div_prefix(k_lo - 1, Cu)) * Hkv;
+          if (k > Cu) {
+            const unsigned k_s = k_lo > Cu + 1 ? k_lo : Cu + 1;
+            pt = seq_off[3 * b + 1] + (int)(ceil_div_prefix(k - 1, Cu) - ceil_div_prefix(k_s - 1, Cu)) * Hkv;
+            split_rows[seq_off[3 * b + 2] + (int)(k - k_s)] = r;
+          }
+        }
+      }
       row_seq[r] = bb;
       item_begin[r] = it;
-      part_begin[r] = n > 1 ? pt : -1;
-      if (n > 1) split_rows[sp++] = r;
-      it += n * a.Hkv;
-      if (n > 1) pt += n * a.Hkv;
-    });
+      part_begin[r] = pt;
+    }
   }
-  const int carry_items = tot[0], carry_parts = tot[1], carry_split = tot[2];
+  const int carry_items = carry[0], carry_parts = carry[1], carry_split = carry[2];
   if (tid == 0) item_begin[a.T] = carry_items;
 
   // pass 3: (sequence, q tile) pairs of the prefill kernel, longest first
@@ -269,7 +303,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
     const int b = base + tid;
     int n = 0;
     if (b < a.B) {
-      const SeqInfo s = seq_info(a, b);
+      const SeqInfo s = seq_info(a, b, partition_bad);
       if (s.tc) n = (s.q + TC_BM - 1) / TC_BM;
     }
     int t;
@@ -286,7 +320,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
     auto pair_work = [&](int p, int* b_out, int* qt_out) {
       const int b = upper_bound_written(pair_begin, a.B + 1, p) - 1;   // shared memory when B fits
       const int qt = p - pair_begin[b];
-      const SeqInfo s = seq_info(a, b);
+      const SeqInfo s = seq_info(a, b, false);
       const int q1 = min(s.q, (qt + 1) * TC_BM);
       const int keys = s.L - s.q + q1;  // keys the tile's last row sees
       int w = (keys + TC_BN - 1) / TC_BN;
@@ -344,9 +378,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
   static cudaError_t attr = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (3 * PLAN_SMEM_SEQS + 2) * 4);
+                                                 (6 * PLAN_SMEM_SEQS + 2) * 4);
   if (attr != cudaSuccess) return attr;
-  const size_t smem = a.B <= PLAN_SMEM_SEQS ? (size_t)(3 * a.B + 2) * 4 : 0;
+  const size_t smem = a.B <= PLAN_SMEM_SEQS ? (size_t)(6 * a.B + 2) * 4 : 0;
   KernelTimer timer("plan", s);
   // may overlap the preceding append, which it does not read (see pdl_wait above)
   cudaError_t e = launch_after_trigger(plan_kernel, dim3(1), dim3(1024), smem, s, a, a.dev_status);

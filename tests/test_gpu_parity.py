@@ -252,6 +252,55 @@ def test_bad_lengths_set_status(dev):
     assert binding.device_status() & binding.DEV_BAD_LENGTHS
 
 
+
+def _attend_after_append(w, dev, kv_lens=None, cu=None):
+    """Caches appended on the host by the oracle; attention alone on the device
+    with (possibly altered) lengths, into an output pre-filled with 7.0."""
+    vals = W.host_values(w)
+    ql, kl, pg = lists(w)
+    packed = binding.pack_tick(ql, kl, pg, w.shape.page_size, w.num_pages)
+    kc_h, vc_h = oracle.kv_append(vals.k_cache, vals.v_cache, vals.k_new, vals.v_new, packed["slot_mapping"])
+    dt = w.shape.dtype
+    out = torch.full((w.total_q, w.shape.num_q_heads, w.shape.head_dim), 7.0, dtype=W.torch_dtype(dt), device=dev)
+    binding.paged_attention(to_dev(vals.q, dt, dev), idx_dev(packed["cu_seqlens_q"] if cu is None else cu, dev),
+                            idx_dev(packed["kv_lens"] if kv_lens is None else kv_lens, dev),
+                            idx_dev(packed["page_tables"], dev), to_dev(kc_h, dt, dev), to_dev(vc_h, dt, dev),
+                            w.scale, w.max_kv_len, out=out)
+    torch.cuda.synchronize()
+    return vals, packed, kc_h, vc_h, out
+
+
+def test_bad_sequence_skipped_others_exact(dev):
+    # long contexts so that the good decode rows are split; sequence 1 too long
+    w = W.random_workload(21, 4, 32, 8, 128, 256, "bf16", (1, 17, 130), 9500)
+    ql, kl, pg = lists(w)
+    packed = binding.pack_tick(ql, kl, pg, w.shape.page_size, w.num_pages)
+    bad_kv = packed["kv_lens"].copy()
+    bad_kv[1] = w.max_kv_len + 1
+    vals, packed, kc_h, vc_h, out = _attend_after_append(w, dev, kv_lens=bad_kv)
+    assert binding.device_status() & binding.DEV_BAD_LENGTHS
+    cu = packed["cu_seqlens_q"]
+    bad_rows = list(range(cu[1], cu[2]))
+    good_rows = [r for r in range(w.total_q) if r not in bad_rows]
+    assert bool((out[bad_rows].float() == 7.0).all())
+    ro, _ = oracle.paged_attention(vals.q, cu, packed["kv_lens"], packed["page_tables"], kc_h, vc_h, w.scale,
+                                   rows=good_rows)
+    eo = float(np.abs(to_host(out[good_rows]).astype(np.float64) - ro).max())
+    assert eo <= TOL_OUT["bf16"], eo
+
+
+def test_decreasing_cu_seqlens_skips_every_row(dev):
+    w = W.random_workload(22, 3, 8, 2, 64, 16, "bf16", (1, 17), 300)
+    ql, kl, pg = lists(w)
+    packed = binding.pack_tick(ql, kl, pg, w.shape.page_size, w.num_pages)
+    cu = packed["cu_seqlens_q"].copy()
+    assert cu[1] < cu[2]
+    cu[1], cu[2] = cu[2], cu[1]              # one q_len < 0: the rows no longer partition
+    _, _, _, _, out = _attend_after_append(w, dev, cu=cu)
+    assert binding.device_status() & binding.DEV_BAD_LENGTHS
+    assert bool((out.float() == 7.0).all())
+    assert binding.device_status() == 0
+
 def test_host_checks_reject_without_launch(dev):
     kc = torch.zeros((4, 16, 2, 64), dtype=torch.bfloat16, device=dev)
     q = torch.zeros((1, 6, 64), dtype=torch.bfloat16, device=dev)   # 6 % 4... Hq=6, Hkv=2 -> g=3 unsupported
