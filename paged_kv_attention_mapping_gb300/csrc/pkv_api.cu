@@ -74,6 +74,11 @@ static cudaEvent_t take_event() {
   return e;
 }
 
+bool kernel_timing_enabled() {
+  std::lock_guard<std::mutex> lk(g_t_mu);
+  return g_timing;
+}
+
 KernelTimer::KernelTimer(const char* name, cudaStream_t s) : name_(name), s_(s), slot_(-1) {
   std::lock_guard<std::mutex> lk(g_t_mu);
   if (!g_timing) return;
@@ -248,6 +253,10 @@ static int attention_impl(const void* q, int q_dtype, const int32_t* cu_seqlens_
   pa.chunk_min = split_chunk_keys(cache->head_dim, elt_bytes(cache->dtype));
   pa.target_items = 1 << 30;
   pa.tc_min_q = tc ? TC_MIN_Q : 0;
+  pa.num_sms = f->num_sms;
+  pa.D = cache->head_dim;
+  pa.kv_elt = elt_bytes(cache->dtype);
+  pa.share_sms = tc && decode_supported(cache->dtype, cache->head_dim, cache->page_size) && !kernel_timing_enabled();
   pa.ws = (char*)workspace;
   pa.lay = lay;
   pa.dev_status = f->status;

@@ -17,6 +17,10 @@ int cuda_fail(cudaError_t e, const char* where);  // records the error text, ret
 // ---------------------------------------------------------------------------
 // kernel timing hooks (pkv_api.cu). A KernelTimer brackets one launch with
 // CUDA events on its stream when timing is enabled.
+// True while per-kernel timing is on: events then sit between the launches,
+// so kernels of one call never overlap.
+bool kernel_timing_enabled();
+
 struct KernelTimer {
   KernelTimer(const char* name, cudaStream_t s);
   ~KernelTimer();
@@ -39,6 +43,7 @@ enum Ctrl : int {
   CTRL_N_SPLIT_ROWS = 6, // rows whose keys were split
   CTRL_N_PARTIALS = 7,   // partial results written
   CTRL_N_PAIRS = 8,      // (seq, q tile) pairs of the prefill kernel
+  CTRL_PF_CTAS = 9,      // prefill-kernel CTAs that take tiles; the SMs of the others run decode CTAs
   CTRL_WORDS = 64
 };
 
@@ -65,6 +70,10 @@ struct PlanArgs {
   int32_t chunk_min;              // smallest split, keys (multiple of 64)
   int32_t target_items;           // aim for about this many row-path items
   int32_t tc_min_q;               // sequences with q_len >= this use the prefill kernel; 0 = never
+  int32_t num_sms;                // SMs of the device
+  int32_t D, kv_elt;              // head_dim and cache element bytes (decode traffic per key)
+  int32_t share_sms;              // 1: the decode kernel can start beside the prefill kernel, so give
+                                  //    the prefill kernel only its share of the SMs (CTRL_PF_CTAS)
   char* ws;
   PlanLayout lay;
   int32_t* dev_status;

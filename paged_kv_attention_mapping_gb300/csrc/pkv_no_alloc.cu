@@ -126,6 +126,10 @@ extern "C" int pkv_paged_attention_no_alloc(const void* q, const int32_t* cu_seq
   pa.chunk_min = split_chunk_keys(c->head_dim, elt);
   pa.target_items = 1 << 30;
   pa.tc_min_q = tc ? kTcMinQ : 0;
+  pa.num_sms = su->num_sms;
+  pa.D = c->head_dim;
+  pa.kv_elt = elt;
+  pa.share_sms = tc && decode_supported(c->dtype, c->head_dim, c->page_size) && !kernel_timing_enabled();
   pa.ws = ws;
   pa.lay = lay;
   pa.dev_status = status;

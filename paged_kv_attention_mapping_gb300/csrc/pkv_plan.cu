@@ -158,6 +158,30 @@ __device__ __forceinline__ long long ceil_div_prefix(unsigned K, unsigned C) {
   return (long long)C * m * (m + 1) / 2 + (long long)r * (m + 1);
 }
 
+// How many SMs the prefill kernel keeps when the decode kernel can start on
+// the others at once. Both run until their work is done, so the split aims to
+// make them end together: a prefill work tile (two 128-row query tiles of one
+// sequence and two q heads) costs an SM about as long as streaming
+// TILE_BYTES of decode K/V, and each of its KV steps (128 keys) STEP_BYTES.
+// Those rates were measured on GB300 with 128-wide heads (a KV step ~2.1 us,
+// a tile boundary ~6 us, the decode kernel ~85 GB/s per SM when it has few
+// SMs, close to the HBM limit from about half of them); 64-wide steps take
+// about three quarters as long. The split only moves
+// time between the two kernels: every tile and item is still done once.
+__device__ int prefill_ctas(const PlanArgs& a, int n_pairs, unsigned long long steps,
+                            unsigned long long row_keys) {
+  const int N = a.num_sms;
+  if (!a.share_sms || n_pairs == 0 || row_keys == 0 || N < 3) return N;
+  constexpr double TILE_BYTES = 510e3;
+  const double step_bytes = a.D >= 128 ? 180e3 : 135e3;
+  const double hp = (double)(a.Hq / 2);
+  const double pf = hp * ((double)steps * step_bytes + (double)n_pairs * TILE_BYTES);
+  const double dec = (double)row_keys * a.Hkv * a.D * a.kv_elt * 2.0;
+  int x = (int)(N * pf / (pf + dec) + 0.5);
+  const int lo = (N + 1) / 2;   // the decode kernel saturates HBM with about half the SMs
+  return x < lo ? lo : (x > N ? N : x);
+}
+
 constexpr int PLAN_SMEM_SEQS = 8192;   // sequences whose lengths and offsets are staged in shared memory
 
 __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_status) {
@@ -183,7 +207,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
   volatile int32_t* seq_off = staged ? s_seq + 3 * a_in.B + 2 : (int32_t*)(a.ws + a.lay.seq_offs);
   int2* pairs = (int2*)(a.ws + a.lay.tc_pairs);
 
-  __shared__ unsigned long long s_keys;
+  __shared__ unsigned long long s_keys, s_steps;
   __shared__ int s_err;
   __shared__ int sm[32];
   __shared__ int sm3[3][32];
@@ -198,6 +222,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
   const bool partition_bad = __syncthreads_or(my_desc) != 0 || ends_bad;
   if (tid == 0) {
     s_keys = 0;
+    s_steps = 0;
     s_err = partition_bad ? PKV_DEV_BAD_LENGTHS : 0;
   }
   __syncthreads();
@@ -323,15 +348,18 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
       const SeqInfo s = seq_info(a, b, false);
       const int q1 = min(s.q, (qt + 1) * TC_BM);
       const int keys = s.L - s.q + q1;  // keys the tile's last row sees
-      int w = (keys + TC_BN - 1) / TC_BN;
       *b_out = b;
       *qt_out = qt;
-      return min(w, HIST - 1);
+      return (keys + TC_BN - 1) / TC_BN;
     };
+    unsigned long long my_steps = 0;
     for (int p = tid; p < n_pairs; p += blockDim.x) {
       int b, qt;
-      atomicAdd(&hist[pair_work(p, &b, &qt)], 1);
+      const int w = pair_work(p, &b, &qt);
+      my_steps += (unsigned long long)w;
+      atomicAdd(&hist[min(w, HIST - 1)], 1);
     }
+    if (my_steps) atomicAdd(&s_steps, my_steps);
     __syncthreads();
     // descending exclusive offsets: hist[w] <- number of pairs with work > w
     {
@@ -353,13 +381,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
     __syncthreads();
     for (int p = tid; p < n_pairs; p += blockDim.x) {
       int b, qt;
-      const int w = pair_work(p, &b, &qt);
+      const int w = min(pair_work(p, &b, &qt), HIST - 1);
       const int pos = atomicAdd(&hist[w], 1);
       pairs[pos] = make_int2(b, qt);
     }
     __syncthreads();
   }
   if (tid == 0) {
+    ctrl[CTRL_PF_CTAS] = prefill_ctas(a, n_pairs, s_steps, s_keys);
     ctrl[CTRL_ERR] = s_err;
     ctrl[CTRL_N_ITEMS] = carry_items;
     ctrl[CTRL_ITEM_NEXT] = 0;

@@ -145,6 +145,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // no tile in this call (every CTA reads the same word): leave before any
   // barrier or tensor-memory set-up
   if (*(volatile const int32_t*)&p.ctrl[CTRL_N_TILES] == 0) return;
+  // CTAs past the prefill share leave their SMs to the decode kernel, which
+  // may start as soon as every CTA here has passed pdl_trigger
+  if ((int)blockIdx.x >= *(volatile const int32_t*)&p.ctrl[CTRL_PF_CTAS]) return;
   if (tid == 0) {
     mbar_init(&bar_q, 1);
     for (int s = 0; s < NS; ++s) {
