@@ -60,6 +60,7 @@ struct DecParams {
   int32_t* dev_status;
   const float* k_scale;  // fp8 caches: dequantisation scale per KV head (else null)
   const float* v_scale;
+  int wait_first;        // launched right after the plan kernel: wait for it before reading the plan
 };
 
 struct Item {
@@ -251,6 +252,8 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (p.wait_first) pdl_wait();
+  pdl_trigger();   // the combine kernel may get resident now; it waits for this grid to finish
   // no item in this call (every CTA reads the same word): leave before any
   // barrier set-up
   if (*(volatile const int32_t*)&p.ctrl[CTRL_N_ITEMS] == 0) {
@@ -1004,17 +1007,16 @@ cudaError_t launch_dec(const AttnArgs& a, cudaStream_t s) {
   p.dev_status = a.dev_status;
   p.k_scale = a.k_scale;
   p.v_scale = a.v_scale;
-  if (a.after_prefill) {
-    // rows of the decode path and tiles of the prefill kernel are disjoint, and
-    // the plan both read finished before the prefill kernel started: this grid
-    // may start as soon as the prefill kernel has (its CTAs fill SMs that the
-    // prefill kernel's tail leaves idle)
-    const cudaError_t e = launch_after_trigger(decode_kernel<T, TKV, D, G>, dim3(a.num_sms * C::CPS),
-                                               dim3(NTHREADS), C::SMEM, s, mk, mv, p);
-    if (e != cudaSuccess) return e;
-  } else {
-    decode_kernel<T, TKV, D, G><<<a.num_sms * C::CPS, NTHREADS, C::SMEM, s>>>(mk, mv, p);
-  }
+  // After the prefill kernel: rows of the decode path and tiles of the prefill
+  // kernel are disjoint, and the plan both read finished before the prefill
+  // kernel started, so this grid may start as soon as the prefill kernel has
+  // (its CTAs take the SMs the prefill kernel leaves) and waits for it only
+  // before it exits. Right after the plan kernel (which triggers at its
+  // start): the CTAs get resident during the plan and wait for it first.
+  p.wait_first = a.after_prefill ? 0 : 1;
+  const cudaError_t e = launch_after_trigger(decode_kernel<T, TKV, D, G>, dim3(a.num_sms * C::CPS),
+                                             dim3(NTHREADS), C::SMEM, s, mk, mv, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

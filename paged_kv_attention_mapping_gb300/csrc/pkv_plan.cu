@@ -187,6 +187,7 @@ constexpr int PLAN_SMEM_SEQS = 8192;   // sequences whose lengths and offsets ar
 __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_status) {
   // stage cu_seqlens_q and kv_lens in shared memory: every row below searches them
   extern __shared__ int32_t s_seq[];
+  pdl_trigger();   // a decode kernel launched next may get resident; it waits for this grid
   PlanArgs a = a_in;
   const bool staged = a_in.B <= PLAN_SMEM_SEQS;
   if (staged) {

@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnArgs a) {
   constexpr int DPL = D / 32;
   using V = typename std::conditional<DPL == 4, float4, float2>::type;
   const int lane = threadIdx.x & 31;
+  pdl_wait();   // launched to overlap the end of the decode kernel, whose partials it reads
   const int32_t* ctrl = (const int32_t*)(a.ws + a.lay.ctrl);
   const int32_t* item_begin = (const int32_t*)(a.ws + a.lay.row_item_begin);
   const int32_t* part_begin = (const int32_t*)(a.ws + a.lay.row_part_begin);
@@ -267,8 +268,11 @@ cudaError_t launch_rows(const AttnArgs& a, cudaStream_t s) {
 template <typename T>
 static cudaError_t launch_combine_t(const AttnArgs& a, cudaStream_t s) {
   const int blocks = a.num_sms * 2;
-  if (a.D == 64) combine_kernel<T, 64><<<blocks, 256, 0, s>>>(a);
-  else combine_kernel<T, 128><<<blocks, 256, 0, s>>>(a);
+  // the grid may get resident once the decode kernel's CTAs have all started;
+  // it waits for that grid to finish before reading the partials
+  const cudaError_t e = a.D == 64 ? launch_after_trigger(combine_kernel<T, 64>, dim3(blocks), dim3(256), 0, s, a)
+                                  : launch_after_trigger(combine_kernel<T, 128>, dim3(blocks), dim3(256), 0, s, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
