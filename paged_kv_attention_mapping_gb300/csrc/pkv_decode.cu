@@ -361,34 +361,32 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
           ok = false;
           break;
         }
-        if (lane == 0) {
-          unsigned char* kdst = sStage + st * C::STAGE_BYTES;
-          unsigned char* vdst = kdst + C::TILE_BYTES;
-          if (bad) {
+        // The copies of a tile are issued by several lanes at once, one copy
+        // (page, K or V, 128-byte atom) per lane, after lane 0 has armed the
+        // barrier.
+        unsigned char* kdst = sStage + st * C::STAGE_BYTES;
+        unsigned char* vdst = kdst + C::TILE_BYTES;
+        if (bad) {
+          if (lane == 0) {
             s_bad[slot] = 1;
             mbar_arrive(&bar_full[st]);
-          } else if (p.P >= BT) {
-            const int row = page[0] * p.P + (kb - lp0 * p.P);
-            mbar_arrive_expect_tx(&bar_full[st], 2 * C::TILE_BYTES);
+          }
+        } else {
+          const int n_copies = npg * 2 * C::ATOMS;
+          if (lane == 0)
+            mbar_arrive_expect_tx(&bar_full[st], (uint32_t)(2 * npg * C::ROW_BYTES * (p.P >= BT ? BT : p.P)));
+          __syncwarp();
+          constexpr int MAX_COPIES = (BT / 8) * 2 * C::ATOMS;
 #pragma unroll
-            for (int a = 0; a < C::ATOMS; ++a) {
-              tma_load_3d(kdst + a * BT * 128, &mk, &bar_full[st], a * C::ATOM_ELEMS, item.kvh, row);
-              tma_load_3d(vdst + a * BT * 128, &mv, &bar_full[st], a * C::ATOM_ELEMS, item.kvh, row);
-            }
-          } else {
-            mbar_arrive_expect_tx(&bar_full[st], (uint32_t)(2 * npg * p.P * C::ROW_BYTES));
-#pragma unroll
-            for (int pp = 0; pp < BT / 8; ++pp) {
-              if (pp < npg) {
-                const int row = page[pp] * p.P;
-#pragma unroll
-                for (int a = 0; a < C::ATOMS; ++a) {
-                  tma_load_3d(kdst + a * BT * 128 + pp * p.P * 128, &mk, &bar_full[st], a * C::ATOM_ELEMS,
-                              item.kvh, row);
-                  tma_load_3d(vdst + a * BT * 128 + pp * p.P * 128, &mv, &bar_full[st], a * C::ATOM_ELEMS,
-                              item.kvh, row);
-                }
-              }
+          for (int base = 0; base < MAX_COPIES; base += 32) {
+            const int idx = base + lane;
+            const int pp = idx / (2 * C::ATOMS), a = (idx >> 1) % C::ATOMS;
+            const int pid = __shfl_sync(0xffffffffu, pg, (lp0 + pp - wb) & 31);   // page of logical page lp0 + pp
+            if (idx < n_copies) {
+              const int row = p.P >= BT ? pid * p.P + (kb - lp0 * p.P) : pid * p.P;
+              const uint32_t off = a * BT * 128 + pp * p.P * 128;
+              if (idx & 1) tma_load_3d(vdst + off, &mv, &bar_full[st], a * C::ATOM_ELEMS, item.kvh, row);
+              else tma_load_3d(kdst + off, &mk, &bar_full[st], a * C::ATOM_ELEMS, item.kvh, row);
             }
           }
         }
