@@ -257,6 +257,9 @@ static int attention_impl(const void* q, int q_dtype, const int32_t* cu_seqlens_
   pa.D = cache->head_dim;
   pa.kv_elt = elt_bytes(cache->dtype);
   pa.share_sms = tc && decode_supported(cache->dtype, cache->head_dim, cache->page_size) && !kernel_timing_enabled();
+  pa.page_tables = page_tables;
+  pa.max_pages = max_pages_per_seq;
+  pa.P = cache->page_size;
   pa.ws = (char*)workspace;
   pa.lay = lay;
   pa.dev_status = f->status;

@@ -54,6 +54,7 @@ struct DecParams {
   int32_t* ctrl;
   const int32_t* item_begin;
   const int32_t* row_seq;
+  const int32_t* row_keys;   // keys each packed row sees (row-path rows)
   const int32_t* part_begin;
   float* part_o;
   float* part_lse;
@@ -256,7 +257,9 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
   pdl_trigger();   // the combine kernel may get resident now; it waits for this grid to finish
   // no item in this call (every CTA reads the same word): leave before any
   // barrier set-up
-  if (*(volatile const int32_t*)&p.ctrl[CTRL_N_ITEMS] == 0) {
+  const int n_items = *(volatile const int32_t*)&p.ctrl[CTRL_N_ITEMS];
+  const int Cchunk = *(volatile const int32_t*)&p.ctrl[CTRL_CHUNK];
+  if (n_items == 0) {
     pdl_wait();
     return;
   }
@@ -275,8 +278,6 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
     s_abort = 0;
   }
   __syncthreads();
-  const int n_items = *(volatile int32_t*)&p.ctrl[CTRL_N_ITEMS];
-  const int Cchunk = *(volatile int32_t*)&p.ctrl[CTRL_CHUNK];
 
   if (warp == NCW) {
     // ================================================================ producer
@@ -292,8 +293,13 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
                                              p.dev_status)))
         break;
       // next item, decoded by the whole warp (few dependent loads)
-      int i = 0;
-      if (lane == 0) i = s_abort ? n_items : atomicAdd(&p.ctrl[CTRL_ITEM_NEXT], 1);
+      // When every CTA starts at once (not beside the prefill kernel, whose SMs
+      // some CTAs wait for), the first item of CTA c is item c and the counter
+      // hands out the rest; otherwise the counter hands out every item.
+      const int first_static = p.wait_first ? (int)gridDim.x : 0;
+      int i = (int)blockIdx.x;
+      if ((it > 0 || !first_static) && lane == 0)
+        i = s_abort ? n_items : first_static + atomicAdd(&p.ctrl[CTRL_ITEM_NEXT], 1);
       i = __shfl_sync(0xffffffffu, i, 0);
       Item item;
       item.valid = 0;
@@ -302,14 +308,11 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
         const int b0 = __ldg(p.item_begin + r);
         const int b1 = __ldg(p.item_begin + r + 1);
         const int b = max(0, __ldg(p.row_seq + r));   // every row with items has its sequence here
-        const int c0 = __ldg(p.cu + b);
-        const int qlen = __ldg(p.cu + b + 1) - c0;
-        const int L = __ldg(p.kv_lens + b);
+        const int limit = __ldg(p.row_keys + r);
         item.local = i - b0;
         item.nsplit = (b1 - b0) / p.Hkv;
         item.kvh = item.local / item.nsplit;
         const int sp = item.local - item.kvh * item.nsplit;
-        const int limit = L - qlen + (r - c0) + 1;
         item.r = r;
         item.b = b;
         item.k0 = sp * Cchunk;
@@ -999,6 +1002,7 @@ cudaError_t launch_dec(const AttnArgs& a, cudaStream_t s) {
   p.ctrl = (int32_t*)(a.ws + a.lay.ctrl);
   p.item_begin = (const int32_t*)(a.ws + a.lay.row_item_begin);
   p.row_seq = (const int32_t*)(a.ws + a.lay.row_seq);
+  p.row_keys = (const int32_t*)(a.ws + a.lay.row_keys);
   p.part_begin = (const int32_t*)(a.ws + a.lay.row_part_begin);
   p.part_o = (float*)(a.ws + a.lay.part_o);
   p.part_lse = (float*)(a.ws + a.lay.part_lse);

@@ -48,7 +48,7 @@ enum Ctrl : int {
 };
 
 struct PlanLayout {
-  size_t ctrl, row_seq, row_item_begin, row_part_begin, split_rows, seq_pair_begin, seq_offs, tc_pairs,
+  size_t ctrl, row_seq, row_keys, row_item_begin, row_part_begin, split_rows, seq_pair_begin, seq_offs, tc_pairs,
       part_lse, part_o, total;
   int32_t partial_cap;  // partial results the workspace can hold
   int32_t pair_cap;     // (seq, q tile) pairs the workspace can hold
@@ -74,6 +74,8 @@ struct PlanArgs {
   int32_t D, kv_elt;              // head_dim and cache element bytes (decode traffic per key)
   int32_t share_sms;              // 1: the decode kernel can start beside the prefill kernel, so give
                                   //    the prefill kernel only its share of the SMs (CTRL_PF_CTAS)
+  const int32_t* page_tables;     // [B, max_pages]: the row-path sequences' entries are prefetched into L2
+  int32_t max_pages, P;
   char* ws;
   PlanLayout lay;
   int32_t* dev_status;

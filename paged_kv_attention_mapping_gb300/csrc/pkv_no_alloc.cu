@@ -130,6 +130,9 @@ extern "C" int pkv_paged_attention_no_alloc(const void* q, const int32_t* cu_seq
   pa.D = c->head_dim;
   pa.kv_elt = elt;
   pa.share_sms = tc && decode_supported(c->dtype, c->head_dim, c->page_size) && !kernel_timing_enabled();
+  pa.page_tables = page_tables;
+  pa.max_pages = max_pages_per_seq;
+  pa.P = c->page_size;
   pa.ws = ws;
   pa.lay = lay;
   pa.dev_status = status;

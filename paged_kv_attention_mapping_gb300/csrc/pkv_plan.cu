@@ -25,6 +25,7 @@ PlanLayout plan_layout(int32_t B, int32_t T, int32_t Hq, int32_t Hkv, int32_t D,
   size_t off = 0;
   L.ctrl = off;            off += align256(CTRL_WORDS * 4);
   L.row_seq = off;         off += align256((size_t)T * 4 + 4);
+  L.row_keys = off;        off += align256((size_t)T * 4 + 4);
   L.row_item_begin = off;  off += align256(((size_t)T + 1) * 4);
   L.row_part_begin = off;  off += align256((size_t)T * 4 + 4);
   L.split_rows = off;      off += align256((size_t)T * 4 + 4);
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
   }
   int32_t* ctrl = (int32_t*)(a.ws + a.lay.ctrl);
   int32_t* row_seq = (int32_t*)(a.ws + a.lay.row_seq);
+  int32_t* row_keys = (int32_t*)(a.ws + a.lay.row_keys);
   int32_t* item_begin = (int32_t*)(a.ws + a.lay.row_item_begin);
   int32_t* part_begin = (int32_t*)(a.ws + a.lay.row_part_begin);
   int32_t* split_rows = (int32_t*)(a.ws + a.lay.split_rows);
@@ -270,6 +272,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
       if (b < B) {
         const SeqInfo s = seq_info(a, b, partition_bad);
         if (!s.bad && !s.tc && s.q > 0) {
+          if (guard == 0 && a.page_tables) {
+            // the decode kernel reads these entries at the start of each item
+            const char* t0 = (const char*)(a.page_tables + (int64_t)b * a.max_pages);
+            const int bytes = ((s.L + a.P - 1) / a.P) * 4;
+            for (int off = 0; off < bytes; off += 128) prefetch_l2(t0 + off);
+          }
           const unsigned k_lo = (unsigned)(s.L - s.q + 1), k_hi = (unsigned)s.L;
           const long long f_hi = ceil_div_prefix(k_hi, Cu);
           cnt[0] = (int)(f_hi - ceil_div_prefix(k_lo - 1, Cu)) * Hkv;
@@ -299,7 +307,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
   {
     const unsigned Cu = (unsigned)C;
     for (int r = tid; r < a.T; r += blockDim.x) {
-      int bb = -1, it = 0, pt = -1;
+      int bb = -1, it = 0, pt = -1, keys = 0;
       if (!partition_bad) {
         const int b = upper_bound_i32(a.cu, B + 1, r) - 1;   // cu[b] <= r < cu[b + 1]
         const SeqInfo s = seq_info(a, b, false);
@@ -307,6 +315,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
         if (!s.bad && !s.tc) {
           bb = b;
           const unsigned k_lo = (unsigned)(s.L - s.q + 1), k = k_lo + (unsigned)(r - s.c0);
+          keys = (int)k;
           it += (int)(ceil_div_prefix(k - 1, Cu) - ceil_div_prefix(k_lo - 1, Cu)) * Hkv;
           if (k > Cu) {
             const unsigned k_s = k_lo > Cu + 1 ? k_lo : Cu + 1;
@@ -316,6 +325,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
         }
       }
       row_seq[r] = bb;
+      row_keys[r] = keys;
       item_begin[r] = it;
       part_begin[r] = pt;
     }
