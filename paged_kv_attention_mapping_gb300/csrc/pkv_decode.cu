@@ -66,7 +66,7 @@ struct DecParams {
 
 struct Item {
   int valid;
-  int r, kvh, b, k0, k1, nsplit, local;
+  int r, kvh, b, k0, k1, nsplit, local;   // local: partial slot of the item within its row (KV head, split)
   int n_tiles;
 };
 
@@ -211,10 +211,22 @@ struct DCfg {
   static constexpr int CPS = (STAGE_BYTES <= 16384 && ELT <= 2 && G <= 8) ? PKV_DEC_CPS_SMALL : 2;
   static constexpr int BASE_NST = STAGE_BYTES <= 32768 ? 3 : 2;
   // 228 KB of shared memory per SM, 1 KB of it reserved per CTA, ~0.5 KB static
-  static constexpr int FIT_NST = (233472 / CPS - 1536 - Q_BYTES - MERGE_BYTES - 1024) / STAGE_BYTES;
-  static constexpr int NST = CPS > 2 ? (FIT_NST < 6 ? FIT_NST : 6)
-                                     : (FIT_NST > BASE_NST ? (FIT_NST < 6 ? FIT_NST : 6) : BASE_NST);
-  static constexpr int SMEM = NST * STAGE_BYTES + Q_BYTES + MERGE_BYTES + 1024;
+  static constexpr int nst_for(int merge_smem) {
+    const int fit = (233472 / CPS - 1536 - Q_BYTES - merge_smem - 1024) / STAGE_BYTES;
+    return CPS > 2 ? (fit < 6 ? fit : 6) : (fit > BASE_NST ? (fit < 6 ? fit : 6) : BASE_NST);
+  }
+  static constexpr int SEP_SMEM = nst_for(MERGE_BYTES) * STAGE_BYTES + Q_BYTES + MERGE_BYTES + 1024;
+  // The warps' states are merged in a buffer of their own, unless that buffer
+  // would keep CPS CTAs from fitting on an SM (head_dim 128 with 8 q heads per
+  // KV head); then they are merged in the stage of the item's last tile, which
+  // is released only after the merge. (Measured: merging in the stage where
+  // the buffer fits anyway was slower.)
+  static constexpr int IN_STAGE_SMEM = nst_for(0) * STAGE_BYTES + Q_BYTES + 1024;
+  static constexpr bool MERGE_IN_STAGE = MERGE_BYTES <= STAGE_BYTES && CPS * (SEP_SMEM + 1536) > 233472 &&
+                                         CPS * (IN_STAGE_SMEM + 1536) <= 233472;
+  static constexpr int MERGE_SMEM = MERGE_IN_STAGE ? 0 : MERGE_BYTES;
+  static constexpr int NST = nst_for(MERGE_SMEM);
+  static constexpr int SMEM = NST * STAGE_BYTES + Q_BYTES + MERGE_SMEM + 1024;
   static constexpr int DPL = D / 32;                   // PV: dims per lane
   static_assert(ROW_BYTES % 128 == 0, "key rows must be whole swizzle atoms");
 };
@@ -309,10 +321,15 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
         const int b1 = __ldg(p.item_begin + r + 1);
         const int b = max(0, __ldg(p.row_seq + r));   // every row with items has its sequence here
         const int limit = __ldg(p.row_keys + r);
-        item.local = i - b0;
+        // a row's items run split by split, the KV heads of one split next to
+        // each other, so that the heads of the same pages are read at about
+        // the same time (the heads of a key row share its DRAM pages); the
+        // partial slots stay ordered (KV head, split)
+        const int j = i - b0;
         item.nsplit = (b1 - b0) / p.Hkv;
-        item.kvh = item.local / item.nsplit;
-        const int sp = item.local - item.kvh * item.nsplit;
+        const int sp = j / p.Hkv;
+        item.kvh = j - sp * p.Hkv;
+        item.local = item.kvh * item.nsplit + sp;
         item.r = r;
         item.b = b;
         item.k0 = sp * Cchunk;
@@ -419,6 +436,18 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
     const bool ok = wait_flag(&bar_cw, cw_phase & 1, &s_abort, p.ctrl, p.dev_status);
     ++cw_phase;
     return __all_sync(0xffffffffu, ok);
+  };
+  // With MERGE_IN_STAGE the merge buffers are the stage of the item's last
+  // tile: wait until every warp is done reading it.
+  uint32_t merge_st = 0;
+  auto merge_into_last_stage = [&]() -> bool {
+    if constexpr (C::MERGE_IN_STAGE) {
+      merge_st = (stage_use - 1) % C::NST;
+      sMergeO = reinterpret_cast<float*>(sStage + merge_st * C::STAGE_BYTES);
+      sMergeML = sMergeO + NCW * G * D;
+      return cw_sync();
+    }
+    return true;
   };
   const uint32_t stage0 = smem_u32(sStage);
   const int grp = lane >> 2, tig = lane & 3;   // mma fragment coordinates
@@ -572,11 +601,12 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
           if (nvalid < 16) fence_proxy_async_smem();   // our zeroing before the next TMA write
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_empty[st]);
+        if (lane == 0 && !(C::MERGE_IN_STAGE && t == item.n_tiles - 1)) mbar_arrive(&bar_empty[st]);
       }
       bad = s_bad[slot] != 0;                          // final once the item's last tile landed
       if (lane == 0) mbar_arrive(&bar_iempty[slot]);   // the item slot may be refilled
       if (!__all_sync(0xffffffffu, ok)) break;
+      if (!merge_into_last_stage()) break;
       // this warp's state into shared memory
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
@@ -769,11 +799,12 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
           if (nvalid < 16) fence_proxy_async_smem();   // our zeroing before the next TMA write
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_empty[st]);
+        if (lane == 0 && !(C::MERGE_IN_STAGE && t == item.n_tiles - 1)) mbar_arrive(&bar_empty[st]);
       }
       bad = s_bad[slot] != 0;                          // final once the item's last tile landed
       if (lane == 0) mbar_arrive(&bar_iempty[slot]);   // the item slot may be refilled
       if (!__all_sync(0xffffffffu, ok)) break;
+      if (!merge_into_last_stage()) break;
       // this warp's state into shared memory
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
@@ -908,11 +939,12 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_empty[st]);
+        if (lane == 0 && !(C::MERGE_IN_STAGE && t == item.n_tiles - 1)) mbar_arrive(&bar_empty[st]);
       }
       bad = s_bad[slot] != 0;
       if (lane == 0) mbar_arrive(&bar_iempty[slot]);
       if (!__all_sync(0xffffffffu, ok)) break;
+      if (!merge_into_last_stage()) break;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         float l = l_part[h];
@@ -958,6 +990,13 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
     } else if (tid == 0) {
       atomicOr(&p.ctrl[CTRL_ERR], PKV_DEV_BAD_PAGE);
       atomicOr(p.dev_status, PKV_DEV_BAD_PAGE);
+    }
+    if constexpr (C::MERGE_IN_STAGE) {
+      // this warp is done with the merge buffers: hand the stage back (the
+      // fence orders our generic writes before the next TMA write into it)
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_empty[merge_st]);
     }
   }
   // When launched to overlap the prefill kernel, finish only after it, so that

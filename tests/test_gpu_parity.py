@@ -117,6 +117,8 @@ RAGGED = [
     (13, 3, 32, 2, 128, 256, "bf16", (130, 1), 500),    # g = 16: eight head pairs per KV head in the prefill kernel
     (14, 3, 8, 4, 64, 64, "f16", (150, 1), 400),        # g = 2, page 64: one page per decode tile
     (15, 3, 16, 8, 128, 128, "bf16", (140, 1), 600),    # page 128 = one prefill KV tile per page
+    (16, 5, 64, 8, 128, 256, "bf16", (1, 2, 17), 2500),  # g = 8 at d 128: warp states merged in a K/V stage; splits
+    (17, 4, 16, 1, 64, 16, "f32", (1, 3), 1200),        # g = 16 fp32: the same merge on the fp32 path; splits
 ]
 
 
