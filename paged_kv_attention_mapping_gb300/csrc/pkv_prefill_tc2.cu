@@ -133,12 +133,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   unsigned char* sQ = sm;                                   // [NWG][Q tile]
   unsigned char* sRing = sQ + NWG * C::Q_BYTES;             // [NS][slot]
 
+  // Work tiles pass through a 2-entry ring (tile t in entry t & 1): the producer
+  // claims tile t + 1 and loads its Q while tile t finishes, so no role waits
+  // for a block-wide barrier between tiles.
   __shared__ __align__(8) uint64_t bar_q, bar_full[NS], bar_empty[NS], bar_sfull[NWG], bar_pfull[NWG],
-      bar_odone[NWG], bar_vfix, bar_drain;
+      bar_odone[NWG], bar_qempty, bar_tfull[2], bar_tempty[2], bar_vfix[2], bar_drain;
   __shared__ uint32_t s_tmem;
-  __shared__ Tile2 s_tile;
+  __shared__ Tile2 s_tile[2];
   __shared__ volatile int s_abort;
-  __shared__ int s_bad;
+  __shared__ int s_bad[2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_trigger();   // the decode kernel that follows reads nothing this kernel writes
@@ -159,7 +162,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&bar_pfull[w], 128);
       mbar_init(&bar_odone[w], 1);
     }
-    mbar_init(&bar_vfix, 1);
+    mbar_init(&bar_qempty, 1);
+    for (int e = 0; e < 2; ++e) {
+      mbar_init(&bar_tfull[e], 1);
+      mbar_init(&bar_tempty[e], 1 + 4 * NWG);   // the MMA thread and every softmax warp
+      mbar_init(&bar_vfix[e], 1);
+    }
     mbar_init(&bar_drain, 1);
     fence_mbar_init();
     s_abort = 0;
@@ -176,48 +184,57 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int n_tiles = *(volatile int32_t*)&p.ctrl[CTRL_N_PAIRS] * hpairs;
   const int g = p.Hq / p.Hkv;
 
-  uint32_t ring = 0;                   // producer / MMA
-  uint32_t p_use[NWG] = {0, 0};        // MMA: P consumed per group
-  uint32_t my_s = 0;                   // softmax thread: S waits of its group
-  uint32_t tile_cnt = 0;
-  uint32_t fills[NS];
+  uint32_t ring = 0;                   // producer / MMA: K/V loads before the current tile
+
+  if (warp == 0) {
+    // --------------------------------------------------------------- producer
+    uint32_t fills[NS];
 #pragma unroll
-  for (int s = 0; s < NS; ++s) fills[s] = 0;
-
-  for (;;) {
-    if (tid == 0) {
-      Tile2 ti;
-      ti.valid = 0;
-      const int t = atomicAdd(&p.ctrl[CTRL_TILE_NEXT], 1);
-      if (t < n_tiles && !s_abort) {
-        const int2 pr = p.pairs[t / hpairs];
-        ti.b = pr.x;
-        ti.h = (t % hpairs) * 2;
-        ti.kvh = ti.h / g;
-        const int c0 = p.cu[ti.b];
-        const int qlen = p.cu[ti.b + 1] - c0;
-        ti.L = p.kv_lens[ti.b];
-        const int q0 = pr.y * BM;
-        ti.row0 = c0 + q0;
-        ti.nr = min(BM, qlen - q0);
-        ti.p_first = ti.L - qlen + q0;
-        const int p_last = ti.p_first + ti.nr - 1;
-        ti.n_kv = (p_last + 1 + BN - 1) / BN;
-        ti.j_mask = (ti.p_first + 1) / BN;
-        ti.zero_from = min(BN, ti.L - (ti.n_kv - 1) * BN);
-        ti.valid = 1;
+    for (int s = 0; s < NS; ++s) fills[s] = 0;
+    bool ok = true;
+    for (uint32_t t = 0; ok; ++t) {
+      const uint32_t e = t & 1;
+      // entry e is free again once every consumer is done with tile t - 2
+      if (t >= 2 &&
+          !__all_sync(0xffffffffu, wait2(&bar_tempty[e], ((t >> 1) - 1) & 1, &s_abort, p.ctrl, p.dev_status))) {
+        ok = false;
+        break;
       }
-      s_tile = ti;
-      s_bad = 0;
-    }
-    __syncthreads();
-    const Tile2 ti = s_tile;
-    if (!ti.valid) break;
-    const int32_t* pt = p.page_tables + (int64_t)ti.b * p.max_pages;
-
-    if (warp == 0) {
-      // ------------------------------------------------------------- producer
-      bool ok = true;
+      if (lane == 0) {
+        Tile2 ti;
+        ti.valid = 0;
+        const int tt = s_abort ? n_tiles : atomicAdd(&p.ctrl[CTRL_TILE_NEXT], 1);
+        if (tt < n_tiles) {
+          const int2 pr = p.pairs[tt / hpairs];
+          ti.b = pr.x;
+          ti.h = (tt % hpairs) * 2;
+          ti.kvh = ti.h / g;
+          const int c0 = p.cu[ti.b];
+          const int qlen = p.cu[ti.b + 1] - c0;
+          ti.L = p.kv_lens[ti.b];
+          const int q0 = pr.y * BM;
+          ti.row0 = c0 + q0;
+          ti.nr = min(BM, qlen - q0);
+          ti.p_first = ti.L - qlen + q0;
+          const int p_last = ti.p_first + ti.nr - 1;
+          ti.n_kv = (p_last + 1 + BN - 1) / BN;
+          ti.j_mask = (ti.p_first + 1) / BN;
+          ti.zero_from = min(BN, ti.L - (ti.n_kv - 1) * BN);
+          ti.valid = 1;
+        }
+        s_tile[e] = ti;
+        s_bad[e] = 0;
+        mbar_arrive(&bar_tfull[e]);   // releases the entry's fields to its waiters
+      }
+      __syncwarp();
+      const Tile2 ti = s_tile[e];
+      if (!ti.valid) break;
+      const int32_t* pt = p.page_tables + (int64_t)ti.b * p.max_pages;
+      // Q of this tile replaces the previous tile's once its last QK MMA is done
+      if (t >= 1 && !__all_sync(0xffffffffu, wait2(&bar_qempty, (t - 1) & 1, &s_abort, p.ctrl, p.dev_status))) {
+        ok = false;
+        break;
+      }
       if (lane == 0) {
         mbar_arrive_expect_tx(&bar_q, NWG * C::Q_BYTES);
 #pragma unroll
@@ -244,7 +261,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               const int off = (j * BN) - lp * p.P;
               const int page = pt[lp];
               if (page < 0 || page >= p.num_pages) {
-                atomicOr(&s_bad, 1);
+                atomicOr(&s_bad[e], 1);
                 mbar_arrive(&bar_full[slot]);
               } else {
                 mbar_arrive_expect_tx(&bar_full[slot], C::SLOT_BYTES);
@@ -262,7 +279,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 bad |= page < 0 || page >= p.num_pages;
               }
               if (bad) {
-                atomicOr(&s_bad, 1);
+                atomicOr(&s_bad[e], 1);
                 mbar_arrive(&bar_full[slot]);
               } else {
                 mbar_arrive_expect_tx(&bar_full[slot], (uint32_t)cnt * p.P * D * 2);
@@ -285,86 +302,150 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               }
               for (int hf = 0; hf < C::HALVES; ++hf) {
                 uint4* base = (uint4*)(dst + hf * BN * 128);
-                for (int e = ti.zero_from * 8 + lane; e < BN * 8; e += 32) base[e] = make_uint4(0, 0, 0, 0);
+                for (int q = ti.zero_from * 8 + lane; q < BN * 8; q += 32) base[q] = make_uint4(0, 0, 0, 0);
               }
               fence_proxy_async_smem();
               __syncwarp();
             }
-            if (lane == 0) mbar_arrive(&bar_vfix);
+            if (lane == 0) mbar_arrive(&bar_vfix[e]);
           }
         }
       }
-      if (!ok && lane == 0) {
-        for (int s = 0; s < NS; ++s)
-          if (fills[s] > 0) mbar_wait(&bar_full[s], (fills[s] - 1) & 1, 500000000ull);
-      }
-    } else if (warp == 1) {
-      // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        const uint32_t id_qk = idesc_f16(BM, BN, BF16, false);
-        const uint32_t id_pv = idesc_f16(BM, D, BF16, true);
-        const uint32_t base = ring;
-        bool ok = wait2(&bar_q, tile_cnt & 1, &s_abort, p.ctrl, p.dev_status);
+    }
+    if (!ok && lane == 0) {
+      for (int s = 0; s < NS; ++s)
+        if (fills[s] > 0) mbar_wait(&bar_full[s], (fills[s] - 1) & 1, 500000000ull);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      // The tensor pipe holds only a few MMAs ahead of this thread, and each
+      // barrier wait or commit here costs on the order of 100 cycles, so the
+      // waits for the next operands sit behind MMAs already queued: K_j after
+      // PV_0 of step j, V_j (used in step j + 1) after PV_1. Ring slots and
+      // parities advance incrementally; descriptors are built once per operand
+      // tile and stepped by constant offsets (the start-address field is the
+      // low 14 bits, and every address stays inside shared memory).
+      const uint32_t id_qk = idesc_f16(BM, BN, BF16, false);
+      const uint32_t id_pv = idesc_f16(BM, D, BF16, true);
+      const uint32_t ring_u32 = smem_u32(sRing);
+      const uint64_t qd = smem_desc(smem_u32(sQ), 16, 1024, LAYOUT_SW128);
+      uint32_t p_use[NWG] = {0, 0};   // P hand-offs consumed per query tile
+      auto issue_qk = [&](int w, uint32_t slot) {
+        const uint64_t kd = smem_desc(ring_u32 + slot * C::SLOT_BYTES, 16, 1024, LAYOUT_SW128);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * BM * 128 + (kk % 4) * 32;
+          const uint32_t offk = (kk / 4) * BN * 128 + (kk % 4) * 32;
+          mma_f16_ss(tmem + w * 128, qd + (uint64_t)((w * C::Q_BYTES + off) >> 4), kd + (uint64_t)(offk >> 4), id_qk,
+                     kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar_sfull[w]);
+      };
+      bool ok = true;
+      for (uint32_t t = 0; ok; ++t) {
+        const uint32_t e = t & 1;
+        if (!wait2(&bar_tfull[e], (t >> 1) & 1, &s_abort, p.ctrl, p.dev_status)) break;
+        const Tile2 ti = s_tile[e];
+        if (!ti.valid) break;
+        // K_j is the tile's load 2j and V_j load 2j + 1 of the ring
+        uint32_t ks = ring % NS, kph = (ring / NS) & 1;
+        uint32_t vs = ks + 1, vph = kph;
+        if (vs == (uint32_t)NS) {
+          vs = 0;
+          vph ^= 1;
+        }
+        ring += 2 * ti.n_kv;
+        ok = wait2(&bar_q, t & 1, &s_abort, p.ctrl, p.dev_status);
         tc_fence_after();
-        // per KV tile j and query tile w: O_w += P_w V_{j-1}, then S_w = Q_w K_j^T
-        for (int j = 0; j <= ti.n_kv && ok; ++j) {
-          const bool qk = j < ti.n_kv, pv = j > 0;
-          const uint32_t ik = base + 2 * j, iv = base + 2 * j - 1;
-          const uint32_t kslot = ik % NS, vslot = iv % NS;
-          if (qk && !wait2(&bar_full[kslot], (ik / NS) & 1, &s_abort, p.ctrl, p.dev_status)) {
+        // step 0: S_w = Q_w K_0^T (the previous tile's last PV, issued earlier,
+        // has read the P held in these columns)
+        if (ok) ok = wait2(&bar_full[ks], kph, &s_abort, p.ctrl, p.dev_status);
+        if (ok) {
+#pragma unroll
+          for (int w = 0; w < NWG; ++w) issue_qk(w, ks);
+          mma_commit(&bar_empty[ks]);
+          if (ti.n_kv == 1) mma_commit(&bar_qempty);
+          ks += 2;
+          if (ks >= (uint32_t)NS) {
+            ks -= NS;
+            kph ^= 1;
+          }
+          ok = wait2(&bar_full[vs], vph, &s_abort, p.ctrl, p.dev_status);
+        }
+        // step j >= 1, per query tile w: O_w (+)= P_w V_{j-1}, then S_w = Q_w K_j^T.
+        // The first PV of a tile overwrites O_w: its P hand-off comes after the
+        // softmax threads have read the previous tile's O_w out of TMEM.
+        for (int j = 1; j <= ti.n_kv && ok; ++j) {
+          const bool qk = j < ti.n_kv;
+          if (j == ti.n_kv && !wait2(&bar_vfix[e], (t >> 1) & 1, &s_abort, p.ctrl, p.dev_status)) {
             ok = false;
             break;
           }
-          if (pv) {
-            if (!wait2(&bar_full[vslot], (iv / NS) & 1, &s_abort, p.ctrl, p.dev_status) ||
-                (j == ti.n_kv && !wait2(&bar_vfix, tile_cnt & 1, &s_abort, p.ctrl, p.dev_status))) {
+          const uint64_t vd = smem_desc(ring_u32 + vs * C::SLOT_BYTES, BN * 128, 1024, LAYOUT_SW128);
+          const uint32_t acc0 = j > 1 ? 1u : 0u;
+          const uint32_t kslot = ks;
+#pragma unroll
+          for (int w = 0; w < NWG; ++w) {
+            if (!wait2(&bar_pfull[w], p_use[w] & 1, &s_abort, p.ctrl, p.dev_status)) {
               ok = false;
               break;
             }
-          }
-          const uint32_t k_base = smem_u32(sRing + kslot * C::SLOT_BYTES);
-          const uint32_t v_base = smem_u32(sRing + vslot * C::SLOT_BYTES);
+            ++p_use[w];
+            tc_fence_after();
 #pragma unroll
-          for (int w = 0; w < NWG; ++w) {
-            if (pv) {
-              if (!wait2(&bar_pfull[w], p_use[w] & 1, &s_abort, p.ctrl, p.dev_status)) {
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_f16_ts(tmem + 256 + w * 128, tmem + w * 128 + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), id_pv,
+                         kk > 0 ? 1u : acc0);
+            if (j == ti.n_kv) mma_commit(&bar_odone[w]);
+            if (w == NWG - 1) {
+              // V_{j-1} has no reader left
+              mma_commit(&bar_empty[vs]);
+              vs += 2;
+              if (vs >= (uint32_t)NS) {
+                vs -= NS;
+                vph ^= 1;
+              }
+            }
+            if (qk) {
+              if (w == 0 && !wait2(&bar_full[kslot], kph, &s_abort, p.ctrl, p.dev_status)) {
                 ok = false;
                 break;
               }
-              ++p_use[w];
-              tc_fence_after();
-#pragma unroll
-              for (int kk = 0; kk < BN / 16; ++kk) {
-                const uint64_t bd = smem_desc(v_base + kk * 16 * 128, BN * 128, 1024, LAYOUT_SW128);
-                mma_f16_ts(tmem + 256 + w * 128, tmem + w * 128 + kk * 8, bd, id_pv, (j > 1 || kk > 0) ? 1u : 0u);
+              if (w == NWG - 1 && !wait2(&bar_full[vs], vph, &s_abort, p.ctrl, p.dev_status)) {
+                ok = false;
+                break;
               }
-              if (j == ti.n_kv) mma_commit(&bar_odone[w]);
-            }
-            if (qk) {
-              const uint32_t q_base = smem_u32(sQ + w * C::Q_BYTES);
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk / 4) * BM * 128 + (kk % 4) * 32;
-                const uint32_t offk = (kk / 4) * BN * 128 + (kk % 4) * 32;
-                mma_f16_ss(tmem + w * 128, smem_desc(q_base + off, 16, 1024, LAYOUT_SW128),
-                           smem_desc(k_base + offk, 16, 1024, LAYOUT_SW128), id_qk, kk > 0 ? 1u : 0u);
-              }
-              mma_commit(&bar_sfull[w]);
+              issue_qk(w, kslot);
             }
           }
           if (!ok) break;
-          if (qk) mma_commit(&bar_empty[kslot]);
-          if (pv) mma_commit(&bar_empty[vslot]);
+          if (qk) {
+            mma_commit(&bar_empty[kslot]);
+            if (j == ti.n_kv - 1) mma_commit(&bar_qempty);
+            ks += 2;
+            if (ks >= (uint32_t)NS) {
+              ks -= NS;
+              kph ^= 1;
+            }
+          }
         }
+        if (ok) mbar_arrive(&bar_tempty[e]);
       }
-      ring += 2 * ti.n_kv;
-    } else {
-      // --------------------------------------------------------------- softmax
-      const int w = (warp - 2) >> 2;                // query tile of this warpgroup
-      const int qq = warp & 3;                      // TMEM lane quarter of this warp
-      const int i = qq * 32 + lane;                 // row within the tile
-      const uint32_t lrow = (uint32_t)(qq * 32) << 16;
-      const uint32_t s_col = w * 128, o_col = 256 + w * 128;
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax
+    const int w = (warp - 2) >> 2;                // query tile of this warpgroup
+    const int qq = warp & 3;                      // TMEM lane quarter of this warp
+    const int i = qq * 32 + lane;                 // row within the tile
+    const uint32_t lrow = (uint32_t)(qq * 32) << 16;
+    const uint32_t s_col = w * 128, o_col = 256 + w * 128;
+    uint32_t my_s = 0;   // S hand-offs consumed by this thread
+    for (uint32_t t = 0;; ++t) {
+      const uint32_t e = t & 1;
+      if (!__all_sync(0xffffffffu, wait2(&bar_tfull[e], (t >> 1) & 1, &s_abort, p.ctrl, p.dev_status))) break;
+      const Tile2 ti = s_tile[e];
+      if (!ti.valid) break;
       const int p_i = min(ti.p_first + i, ti.L - 1);
       const float sc = p.scale_log2;
       float m_run = -INFINITY, l_run = 0.f;
@@ -447,11 +528,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_before();
         mbar_arrive(&bar_pfull[w]);
       }
-      if (ok) ok = __all_sync(0xffffffffu, wait2(&bar_odone[w], tile_cnt & 1, &s_abort, p.ctrl, p.dev_status));
-      if (ok) ok = __all_sync(0xffffffffu, wait2(&bar_vfix, tile_cnt & 1, &s_abort, p.ctrl, p.dev_status));
+      if (ok) ok = __all_sync(0xffffffffu, wait2(&bar_odone[w], t & 1, &s_abort, p.ctrl, p.dev_status));
+      if (ok) ok = __all_sync(0xffffffffu, wait2(&bar_vfix[e], (t >> 1) & 1, &s_abort, p.ctrl, p.dev_status));
       tc_fence_after();
       if (ok) {
-        const bool store = i < ti.nr && !s_bad;
+        const int bad = s_bad[e];
+        const bool store = i < ti.nr && !bad;
         const float inv = 1.f / l_run;
         T* dst = (T*)p.out + ((int64_t)(ti.row0 + i) * p.Hq + ti.h + w) * D;
 #pragma unroll 1
@@ -470,16 +552,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
         if (store && p.lse) p.lse[(int64_t)(ti.row0 + i) * p.Hq + ti.h + w] = (m_run + __log2f(l_run)) * LN2;
-        if (i == 0 && w == 0 && s_bad) {
+        if (i == 0 && w == 0 && bad) {
           atomicOr(&p.ctrl[CTRL_ERR], PKV_DEV_BAD_PAGE);
           atomicOr(p.dev_status, PKV_DEV_BAD_PAGE);
         }
       }
       tc_fence_before();
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_tempty[e]);
     }
-    ++tile_cnt;
-    __syncthreads();
-    if (s_abort) break;
   }
 
   if (warp == 1) {
