@@ -164,17 +164,17 @@ __device__ __forceinline__ long long ceil_div_prefix(unsigned K, unsigned C) {
 // make them end together: a prefill work tile (two 128-row query tiles of one
 // sequence and two q heads) costs an SM about as long as streaming
 // TILE_BYTES of decode K/V, and each of its KV steps (128 keys) STEP_BYTES.
-// Those rates were measured on GB300 with 128-wide heads (a KV step ~2.1 us,
-// a tile boundary ~6 us, the decode kernel ~85 GB/s per SM when it has few
-// SMs, close to the HBM limit from about half of them); 64-wide steps take
-// about three quarters as long. The split only moves
-// time between the two kernels: every tile and item is still done once.
+// Those rates were measured on GB300 with 128-wide heads (a KV step ~1.9 us,
+// the start and end of a work tile ~2.4 us beyond its steps, the decode kernel
+// ~85 GB/s per SM when it has few SMs, close to the HBM limit from about half
+// of them); 64-wide steps take about three quarters as long. The split only
+// moves time between the two kernels: every tile and item is still done once.
 __device__ int prefill_ctas(const PlanArgs& a, int n_pairs, unsigned long long steps,
                             unsigned long long row_keys) {
   const int N = a.num_sms;
   if (!a.share_sms || n_pairs == 0 || row_keys == 0 || N < 3) return N;
-  constexpr double TILE_BYTES = 510e3;
-  const double step_bytes = a.D >= 128 ? 180e3 : 135e3;
+  constexpr double TILE_BYTES = 200e3;
+  const double step_bytes = a.D >= 128 ? 165e3 : 124e3;
   const double hp = (double)(a.Hq / 2);
   const double pf = hp * ((double)steps * step_bytes + (double)n_pairs * TILE_BYTES);
   const double dec = (double)row_keys * a.Hkv * a.D * a.kv_elt * 2.0;
