@@ -14,7 +14,7 @@ once in a CUDA graph and replayed (the library plans on the device, so replays
 need no host work); `eager` reports the same step launched call by call. `e2e` is the same
 metric through the public calls with host buffers: per step the host packs the
 tick, copies its inputs from pinned memory, runs the calls, and reads the
-outputs back, with consecutive steps pipelined over two buffer sets. `--impl reference` times the CPU oracle on a bounded sample of the
+outputs back, with consecutive steps pipelined over three buffer sets. `--impl reference` times the CPU oracle on a bounded sample of the
 same workload instead.
 """
 import argparse
@@ -435,15 +435,25 @@ def main():
 
     # e2e: host buffers through the public calls. Every step packs its tick on
     # the host, copies its inputs and metadata in from pinned memory and reads
-    # out and lse back. Steps are pipelined over two buffer sets, as a serving
+    # out and lse back. Steps are pipelined over three buffer sets, as a serving
     # loop would run them: while the GPU computes step i, step i+1 is packed and
-    # copied in on a second stream and step i-1's outputs go back on a third.
+    # copied in on a second stream and step i-1's outputs go back on a third;
+    # the third set lets step i+1's packing start before step i-1's read-back ends.
     pin = lambda t: t.cpu().pin_memory()
     h_q, h_k, h_v = pin(q), pin(kn), pin(vn)
     meta_keys = ("cu_seqlens_q", "kv_lens", "page_tables", "slot_mapping")
     pk0 = binding.pack_tick(ql, kl, pg, s.page_size, w.num_pages)
+    # the scheduler's view of the tick: flat int32 arrays (lengths, page-table
+    # offsets and page ids), packed every step straight into pinned memory
+    f_ql, f_kl = np.asarray(ql, dtype=np.int32), np.asarray(kl, dtype=np.int32)
+    f_offs = np.zeros(len(pg) + 1, dtype=np.int32)
+    np.cumsum([len(p_) for p_ in pg], out=f_offs[1:])
+    f_ids = np.concatenate([np.asarray(p_, dtype=np.int32) for p_ in pg]) if pg else np.zeros(0, dtype=np.int32)
+    f_width = int(pk0["page_tables"].shape[1])
+    f_order = np.zeros(max(len(ql), 1), dtype=np.int32)
+    NSETS = 3
     sets = []
-    for _ in range(2):
+    for _ in range(NSETS):
         hm = [torch.from_numpy(np.ascontiguousarray(pk0[k])).pin_memory() for k in meta_keys]
         sets.append(dict(q=torch.empty_like(q), k=torch.empty_like(kn), v=torch.empty_like(vn), hmeta=hm,
                          meta=[torch.empty_like(m, device=dev) for m in hm], out=torch.empty_like(out),
@@ -456,11 +466,12 @@ def main():
 
     def e2e_run(n):
         for i in range(n):
-            st = sets[i % 2]
-            st["ev_out"].synchronize()          # step i-2 read back: its host and device buffers are free
-            pk = binding.pack_tick(ql, kl, pg, s.page_size, w.num_pages)
-            for k, hm in zip(meta_keys, st["hmeta"]):
-                hm.numpy()[...] = pk[k]
+            st = sets[i % NSETS]
+            st["ev_out"].synchronize()          # step i-NSETS read back: its host and device buffers are free
+            hm_np = [hm.numpy() for hm in st["hmeta"]]
+            binding.pack_tick_flat(f_ql, f_kl, f_offs, f_ids, s.page_size, w.num_pages, f_width,
+                                   out=dict(order=f_order, cu_seqlens_q=hm_np[0], kv_lens=hm_np[1],
+                                            page_tables=hm_np[2], slot_mapping=hm_np[3]))
             with torch.cuda.stream(s_in):
                 s_in.wait_event(st["ev_done"])
                 for hm, dm in zip(st["hmeta"], st["meta"]):
@@ -538,7 +549,7 @@ def main():
         "e2e": {"value": world * T / (e2e_avg / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_avg,
                 "note": "host packing, H2D of inputs and metadata, the calls and D2H of out/lse every step, "
-                        "pipelined over two buffer sets on three streams; no L2 flush (each step reads more KV "
+                        "pipelined over three buffer sets on three streams; no L2 flush (each step reads more KV "
                         "than L2 holds on the mixed, qwen3 and long workloads)"},
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "clocks": clk.summary(),

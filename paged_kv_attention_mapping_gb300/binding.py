@@ -8,6 +8,7 @@ or cannot be loaded, every call raises.
 from __future__ import annotations
 
 import ctypes
+import itertools
 import os
 from typing import Optional, Sequence
 
@@ -76,7 +77,7 @@ def lib():
     L = ctypes.CDLL(LIB_PATH)
     i32, i64, vp, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
     P32, P64 = ctypes.POINTER(i32), ctypes.POINTER(i64)
-    L.pkv_pack_tick.argtypes = [i32, P32, P32, P32, P32, i32, i32, i32, i32, P32, P32, P32, P32, P64, P32]
+    L.pkv_pack_tick.argtypes = [i32, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
     L.pkv_pack_tick.restype = ctypes.c_int
     L.pkv_kv_append.argtypes = [vp, vp, vp, i32, vp, vp, ctypes.POINTER(CacheDesc), vp]
     L.pkv_kv_append.restype = ctypes.c_int
@@ -155,32 +156,62 @@ def pack_tick(q_lens: Sequence[int], kv_lens: Sequence[int], pages: Sequence[Seq
     """Host packing of one tick (pkv_pack_tick). Returns numpy arrays:
     order, cu_seqlens_q, kv_lens, page_tables [B, W] (-1 padded), slot_mapping."""
     B = len(q_lens)
-    W = int(max_pages_per_seq if max_pages_per_seq is not None else max((len(p) for p in pages), default=1))
-    W = max(W, 1)
+    counts = [len(p) for p in pages]
+    offs = np.zeros(B + 1, dtype=np.int32)
+    if B:
+        np.cumsum(counts, out=offs[1:])
+    ids = np.fromiter(itertools.chain.from_iterable(pages), dtype=np.int32, count=int(offs[-1]))
+    return pack_tick_flat(np.asarray(q_lens, dtype=np.int32), np.asarray(kv_lens, dtype=np.int32), offs, ids,
+                          page_size, num_pages, max_pages_per_seq)
+
+
+def pack_tick_flat(q_lens, kv_lens, page_offsets, page_ids, page_size: int, num_pages: int,
+                   max_pages_per_seq: Optional[int] = None, out: Optional[dict] = None):
+    """pack_tick on flat int32 arrays, the form a scheduler keeps its block
+    tables in: sequence b owns page_ids[page_offsets[b]:page_offsets[b + 1]].
+
+    `out` may hold preallocated (for example pinned) numpy arrays to write into:
+    order [>= B], cu_seqlens_q [B + 1], kv_lens [>= B], page_tables [B, W] and
+    slot_mapping [>= sum of q_lens] (int64), so that a serving loop packs each
+    tick without allocating. Returns the same dict as pack_tick (views of `out`)."""
     ql = np.ascontiguousarray(q_lens, dtype=np.int32)
     kl = np.ascontiguousarray(kv_lens, dtype=np.int32)
-    offs = np.zeros(B + 1, dtype=np.int32)
-    offs[1:] = np.cumsum([len(p) for p in pages]) if B else []
-    ids = np.ascontiguousarray(np.concatenate([np.asarray(p, dtype=np.int32) for p in pages])
-                               if B and offs[-1] > 0 else np.zeros(1, dtype=np.int32), dtype=np.int32)
+    offs = np.ascontiguousarray(page_offsets, dtype=np.int32)
+    ids = np.ascontiguousarray(page_ids, dtype=np.int32)
+    B = int(ql.shape[0])
+    if offs.shape[0] != B + 1:
+        raise ValueError("page_offsets must have num_seqs + 1 entries")
+    if ids.size == 0:
+        ids = np.zeros(1, dtype=np.int32)
+    if max_pages_per_seq is not None:
+        W = int(max_pages_per_seq)
+    else:
+        W = int(np.max(np.diff(offs))) if B else 1
+    W = max(W, 1)
     cap = int(max(int(ql.clip(min=0).sum()), 1))
-    order = np.zeros(max(B, 1), dtype=np.int32)
-    cu = np.zeros(B + 1, dtype=np.int32)
-    kv_out = np.zeros(max(B, 1), dtype=np.int32)
-    tables = np.zeros((max(B, 1), W), dtype=np.int32)
-    slots = np.zeros(cap, dtype=np.int64)
+    if out is None:
+        out = dict(order=np.zeros(max(B, 1), dtype=np.int32), cu_seqlens_q=np.zeros(B + 1, dtype=np.int32),
+                   kv_lens=np.zeros(max(B, 1), dtype=np.int32), page_tables=np.zeros((max(B, 1), W), dtype=np.int32),
+                   slot_mapping=np.zeros(cap, dtype=np.int64))
+    order, cu, kv_out, tables, slots = (out["order"], out["cu_seqlens_q"], out["kv_lens"], out["page_tables"],
+                                        out["slot_mapping"])
+    if (order.dtype != np.int32 or cu.dtype != np.int32 or kv_out.dtype != np.int32 or tables.dtype != np.int32
+            or slots.dtype != np.int64):
+        raise ValueError("pack_tick_flat: out arrays must be int32 (slot_mapping int64)")
+    if (order.size < max(B, 1) or cu.size < B + 1 or kv_out.size < max(B, 1) or tables.ndim != 2
+            or tables.shape[0] < max(B, 1) or tables.shape[1] != W or slots.size < cap):
+        raise ValueError("pack_tick_flat: out arrays too small for this tick")
+    for a in (order, cu, kv_out, tables, slots):
+        if not a.flags.c_contiguous:
+            raise ValueError("pack_tick_flat: out arrays must be C-contiguous")
     total = np.zeros(1, dtype=np.int32)
-    P32 = ctypes.POINTER(ctypes.c_int32)
-
-    def p32(a):
-        return a.ctypes.data_as(P32)
-
-    st = lib().pkv_pack_tick(B, p32(ql) if B else None, p32(kl) if B else None, p32(offs), p32(ids),
-                             int(page_size), int(num_pages), W, cap, p32(order), p32(cu), p32(kv_out),
-                             p32(tables), slots.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), p32(total))
+    st = lib().pkv_pack_tick(B, ql.ctypes.data if B else None, kl.ctypes.data if B else None, offs.ctypes.data,
+                             ids.ctypes.data, int(page_size), int(num_pages), W, cap, order.ctypes.data,
+                             cu.ctypes.data, kv_out.ctypes.data, tables.ctypes.data, slots.ctypes.data,
+                             total.ctypes.data)
     _check(st, "pkv_pack_tick")
     T = int(total[0])
-    return dict(order=order[:B], cu_seqlens_q=cu, kv_lens=kv_out[:B], page_tables=tables[:B],
+    return dict(order=order[:B], cu_seqlens_q=cu[:B + 1], kv_lens=kv_out[:B], page_tables=tables[:B],
                 slot_mapping=slots[:T])
 
 

@@ -79,6 +79,49 @@ def test_pack_tick_matches_oracle_on_named_workloads(lib, name):
         assert np.array_equal(got[k], want[k]), k
 
 
+@pytest.mark.parametrize("seed", range(4))
+def test_pack_tick_flat_into_preallocated_buffers(lib, seed):
+    """The flat-array form writes the oracle's packing into caller buffers, and
+    the same buffers can be reused for the next tick (stale contents overwritten)."""
+    rng = np.random.default_rng(100 + seed)
+    P = int(rng.choice([1, 3, 16]))
+    q_lens, kv, pages, n_pages = _rand_requests(rng, int(rng.integers(1, 12)), P)
+    B = len(q_lens)
+    width = max(len(p) for p in pages) + int(rng.integers(0, 3))
+    offs = np.zeros(B + 1, dtype=np.int32)
+    offs[1:] = np.cumsum([len(p) for p in pages])
+    ids = np.concatenate([np.asarray(p, dtype=np.int32) for p in pages])
+    cap = max(sum(max(q, 0) for q in q_lens), 1)
+    out = dict(order=np.full(B, 77, np.int32), cu_seqlens_q=np.full(B + 1, 77, np.int32),
+               kv_lens=np.full(B, 77, np.int32), page_tables=np.full((B, width), 77, np.int32),
+               slot_mapping=np.full(cap, 77, np.int64))
+    want = oracle.pack_tick(q_lens, kv, pages, P, width)
+    for _ in range(2):
+        got = binding.pack_tick_flat(q_lens, kv, offs, ids, P, n_pages, width, out=out)
+        for k in ("order", "cu_seqlens_q", "kv_lens", "page_tables", "slot_mapping"):
+            assert np.array_equal(got[k], want[k]), k
+            assert np.shares_memory(got[k], out[k]), k
+    fresh = binding.pack_tick_flat(q_lens, kv, offs, ids, P, n_pages, width)
+    for k in want:
+        assert np.array_equal(fresh[k], want[k]), k
+
+
+def test_pack_tick_flat_rejects_small_or_mistyped_buffers(lib):
+    offs = np.array([0, 1, 2], np.int32)
+    ids = np.array([0, 1], np.int32)
+    good = dict(order=np.zeros(2, np.int32), cu_seqlens_q=np.zeros(3, np.int32), kv_lens=np.zeros(2, np.int32),
+                page_tables=np.zeros((2, 1), np.int32), slot_mapping=np.zeros(2, np.int64))
+    binding.pack_tick_flat([1, 1], [3, 3], offs, ids, 4, 2, 1, out=good)
+    for key, bad in (("slot_mapping", np.zeros(1, np.int64)), ("slot_mapping", np.zeros(2, np.int32)),
+                     ("page_tables", np.zeros((2, 2), np.int32)), ("cu_seqlens_q", np.zeros(2, np.int32))):
+        o = dict(good)
+        o[key] = bad
+        with pytest.raises(ValueError):
+            binding.pack_tick_flat([1, 1], [3, 3], offs, ids, 4, 2, 1, out=o)
+    with pytest.raises(ValueError):
+        binding.pack_tick_flat([1, 1], [3, 3], offs[:2], ids, 4, 2, 1)
+
+
 def test_pack_tick_rejects_bad_inputs(lib):
     ok = dict(q_lens=[1, 3], kv_lens=[4, 3], pages=[[0], [1]], page_size=4, num_pages=2)
 
