@@ -173,12 +173,14 @@ __device__ int prefill_ctas(const PlanArgs& a, int n_pairs, unsigned long long s
                             unsigned long long row_keys) {
   const int N = a.num_sms;
   if (!a.share_sms || n_pairs == 0 || row_keys == 0 || N < 3) return N;
-  constexpr double TILE_BYTES = 200e3;
-  const double step_bytes = a.D >= 128 ? 165e3 : 124e3;
-  const double hp = (double)(a.Hq / 2);
-  const double pf = hp * ((double)steps * step_bytes + (double)n_pairs * TILE_BYTES);
-  const double dec = (double)row_keys * a.Hkv * a.D * a.kv_elt * 2.0;
-  int x = (int)(N * pf / (pf + dec) + 0.5);
+  // fp32: this part's fp64 rate is far below its fp32 rate, and a split
+  // estimate needs no more than fp32 precision
+  constexpr float TILE_BYTES = 200e3f;
+  const float step_bytes = a.D >= 128 ? 165e3f : 124e3f;
+  const float hp = (float)(a.Hq / 2);
+  const float pf = hp * ((float)steps * step_bytes + (float)n_pairs * TILE_BYTES);
+  const float dec = (float)row_keys * (float)(a.Hkv * a.D * a.kv_elt) * 2.f;
+  int x = (int)((float)N * pf / (pf + dec) + 0.5f);
   const int lo = (N + 1) / 2;   // the decode kernel saturates HBM with about half the SMs
   return x < lo ? lo : (x > N ? N : x);
 }
@@ -210,7 +212,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
   volatile int32_t* seq_off = staged ? s_seq + 3 * a_in.B + 2 : (int32_t*)(a.ws + a.lay.seq_offs);
   int2* pairs = (int2*)(a.ws + a.lay.tc_pairs);
 
-  __shared__ unsigned long long s_keys, s_steps;
+  // per-warp partial sums (64-bit atomics on shared memory serialise badly)
+  __shared__ unsigned long long s_wkeys[32], s_wsteps[32];
   __shared__ int s_err;
   __shared__ int sm[32];
   __shared__ int sm3[3][32];
@@ -224,8 +227,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
   for (int b = tid; b < B; b += blockDim.x) my_desc |= a.cu[b + 1] < a.cu[b] ? 1 : 0;
   const bool partition_bad = __syncthreads_or(my_desc) != 0 || ends_bad;
   if (tid == 0) {
-    s_keys = 0;
-    s_steps = 0;
     s_err = partition_bad ? PKV_DEV_BAD_LENGTHS : 0;
   }
   __syncthreads();
@@ -245,10 +246,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
     my_err |= __shfl_xor_sync(0xffffffffu, my_err, o);
   }
   if ((tid & 31) == 0) {
-    atomicAdd(&s_keys, my_keys);
+    s_wkeys[tid >> 5] = my_keys;
+    s_wsteps[tid >> 5] = 0;
     if (my_err) atomicOr(&s_err, my_err);
   }
   const bool any_tc = __syncthreads_or(my_tc) != 0;   // no prefill-kernel sequence: skip pass 3
+  unsigned long long s_keys = s_wkeys[tid & 31];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s_keys += __shfl_xor_sync(0xffffffffu, s_keys, o);
   // split size: about target_items items, at least chunk_min keys, multiple of 64
   const long long work = (long long)s_keys * Hkv;
   long long C = (work + a.target_items - 1) / a.target_items;
@@ -370,7 +375,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
       my_steps += (unsigned long long)w;
       atomicAdd(&hist[min(w, HIST - 1)], 1);
     }
-    if (my_steps) atomicAdd(&s_steps, my_steps);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) my_steps += __shfl_xor_sync(0xffffffffu, my_steps, o);
+    if ((tid & 31) == 0) s_wsteps[tid >> 5] = my_steps;
     __syncthreads();
     // descending exclusive offsets: hist[w] <- number of pairs with work > w
     {
@@ -399,7 +406,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
     __syncthreads();
   }
   if (tid == 0) {
-    ctrl[CTRL_PF_CTAS] = prefill_ctas(a, n_pairs, s_steps, s_keys);
+    unsigned long long steps = 0;
+    for (int k = 0; k < 32; ++k) steps += s_wsteps[k];
+    ctrl[CTRL_PF_CTAS] = prefill_ctas(a, n_pairs, steps, s_keys);
     ctrl[CTRL_ERR] = s_err;
     ctrl[CTRL_N_ITEMS] = carry_items;
     ctrl[CTRL_ITEM_NEXT] = 0;
