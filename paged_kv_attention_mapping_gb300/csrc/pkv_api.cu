@@ -233,9 +233,14 @@ static int attention_impl(const void* q, int q_dtype, const int32_t* cu_seqlens_
   if (!f->ok) return PKV_E_DEVICE;
   cudaStream_t s = (cudaStream_t)stream;
 
-  // fp8 caches have no tensor-core prefill kernel yet: their chunk rows take the row path
+  // fp8 caches have no tensor-core prefill kernel yet: their chunk rows take the row path.
+  // A tick with no more rows than sequences is decode-only but for ticks where
+  // all rows sit in one sequence and every other sequence is idle: it skips the
+  // prefill kernel, so the decode kernel gets resident while the plan runs
+  // instead of queueing behind an empty prefill grid (any chunk of such a tick
+  // takes the row path).
   const bool tc = !fp8 && prefill_tc_supported(cache->dtype, cache->head_dim, cache->page_size) &&
-                  total_q >= TC_MIN_Q;
+                  total_q >= TC_MIN_Q && total_q > num_seqs;
 
   PlanArgs pa{};
   pa.cu = cu_seqlens_q;

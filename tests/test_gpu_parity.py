@@ -119,6 +119,10 @@ RAGGED = [
     (15, 3, 16, 8, 128, 128, "bf16", (140, 1), 600),    # page 128 = one prefill KV tile per page
     (16, 5, 64, 8, 128, 256, "bf16", (1, 2, 17), 2500),  # g = 8 at d 128: warp states merged in a K/V stage; splits
     (17, 4, 16, 1, 64, 16, "f32", (1, 3), 1200),        # g = 16 fp32: the same merge on the fp32 path; splits
+    # many short chunks: each prefill CTA runs several 1-2 step work tiles back to
+    # back through its 2-entry tile ring (Q reloads, V-tail fixes, tile hand-offs)
+    (18, 24, 16, 4, 128, 256, "bf16", (64, 128, 129, 200), 600),
+    (19, 24, 32, 4, 64, 16, "f16", (64, 100, 150, 1), 400),
 ]
 
 
