@@ -133,6 +133,25 @@ def test_ragged(dev, case):
     run_and_compare(w, dev)
 
 
+def test_chunk_among_idle_sequences_takes_row_path(dev):
+    """A tick with no more rows than sequences skips the tensor-core prefill
+    kernel; a 64-row chunk whose 63 companions are idle is then attended row by
+    row, with the same results as the oracle."""
+    rng = np.random.default_rng(31)
+    P, B = 16, 64
+    shape = W.TickShape(8, 2, 64, P, "bf16")
+    reqs, pool = [], list(rng.permutation(400))
+    for b in range(B):
+        q = 64 if b == 17 else 0
+        L = 64 + int(rng.integers(1, 120)) if q else int(rng.integers(1, 40))
+        n = (L + P - 1) // P
+        reqs.append(W.Request(q, L, [int(x) for x in pool[:n]]))
+        pool = pool[n:]
+    w = W.Workload("idle_chunk", shape, reqs, 400, 0.125, 31)
+    assert w.total_q == B
+    run_and_compare(w, dev)
+
+
 def test_without_lse(dev):
     w = W.random_workload(11, 4, 8, 2, 64, 16, "bf16", (1, 17), 120)
     run_and_compare(w, dev, want_lse=False)
