@@ -24,6 +24,11 @@
 // 16-bit A operand). O is rescaled in TMEM only when a row's max grows by more
 // than 2^8. P never goes through shared memory, which leaves room for a deep
 // K/V ring.
+// Work tiles follow one another without a block-wide barrier: the producer
+// claims the next tile into a 2-entry ring while the current one runs and
+// reloads Q once the current tile's last QK MMA is done; the MMA thread starts
+// the next tile's first QK while the softmax warps still write the previous
+// tile's output.
 // Every mbarrier wait is bounded (PKV_DEV_TIMEOUT); TMEM accesses are
 // warp-uniform.
 #include <cuda.h>
