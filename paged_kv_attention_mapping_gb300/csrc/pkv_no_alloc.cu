@@ -113,7 +113,10 @@ extern "C" int pkv_paged_attention_no_alloc(const void* q, const int32_t* cu_seq
   cudaStream_t s = (cudaStream_t)stream;
   char* ws = su->scratch;
 
-  const bool tc = prefill_tc_supported(c->dtype, c->head_dim, c->page_size) && total_q >= kTcMinQ;
+  // as in the workspace entry point: a tick with no more rows than sequences
+  // skips the tensor-core prefill kernel
+  const bool tc = prefill_tc_supported(c->dtype, c->head_dim, c->page_size) && total_q >= kTcMinQ &&
+                  total_q > num_seqs;
   PlanArgs pa{};
   pa.cu = cu_seqlens_q;
   pa.kv_lens = kv_lens;
