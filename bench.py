@@ -262,7 +262,7 @@ def run_reference(args):
     per_step = []
     desc = ""
     threads = 1
-    total_budget = 20.0
+    total_budget = args.ref_seconds
     steps = max(1, args.steps)
     secs = max(0.05, total_budget / (steps + args.warmup))   # oracle seconds per step
     for i in range(args.warmup + steps):
@@ -291,6 +291,8 @@ def main():
     ap.add_argument("--workload", default="mixed_tick", choices=list(W.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=20.0,
+                    help="oracle seconds the reference arm spends over all its steps")
     ap.add_argument("--rope", action="store_true",
                     help="rotate Q and K by position in the append (fused RoPE append) before attention")
     ap.add_argument("--kv-fp8", action="store_true",
