@@ -164,18 +164,19 @@ __device__ __forceinline__ long long ceil_div_prefix(unsigned K, unsigned C) {
 // make them end together: a prefill work tile (two 128-row query tiles of one
 // sequence and two q heads) costs an SM about as long as streaming
 // TILE_BYTES of decode K/V, and each of its KV steps (128 keys) STEP_BYTES.
-// Those rates were measured on GB300 with 128-wide heads (a KV step ~1.9 us,
-// the start and end of a work tile ~2.4 us beyond its steps, the decode kernel
-// ~85 GB/s per SM when it has few SMs, close to the HBM limit from about half
-// of them); 64-wide steps take about three quarters as long. The split only
-// moves time between the two kernels: every tile and item is still done once.
+// The constants were fitted on GB300 with 128-wide heads by sweeping them on a
+// mixed tick (a KV step ~1.9 us, the start and end of a work tile less than a
+// step, against a decode kernel that streams ~85-100 GB/s per SM when it has
+// few SMs and nears the HBM limit from about half of them); 64-wide steps take
+// about three quarters as long. The split only moves time between the two
+// kernels: every tile and item is still done once.
 __device__ int prefill_ctas(const PlanArgs& a, int n_pairs, unsigned long long steps,
                             unsigned long long row_keys) {
   const int N = a.num_sms;
   if (!a.share_sms || n_pairs == 0 || row_keys == 0 || N < 3) return N;
   // fp32: this part's fp64 rate is far below its fp32 rate, and a split
   // estimate needs no more than fp32 precision
-  constexpr float TILE_BYTES = 200e3f;
+  constexpr float TILE_BYTES = 80e3f;
   const float step_bytes = a.D >= 128 ? 165e3f : 124e3f;
   const float hp = (float)(a.Hq / 2);
   const float pf = hp * ((float)steps * step_bytes + (float)n_pairs * TILE_BYTES);
