@@ -377,6 +377,16 @@ int pkv_set_kernel_timing(int enable);
  * a negative pkv_status. names[i] points at static storage. */
 int pkv_kernel_times(const char** names, int32_t* launches, double* total_ms, int32_t max);
 
+/* Self-test of the failure path (the pages have no counterpart; it checks the
+ * library's own error handling). Enqueues on `stream` one CTA whose thread
+ * waits, with the bounded mbarrier wait that every kernel of the library uses,
+ * on a barrier that nothing ever completes. After about limit_us microseconds
+ * the wait gives up, the kernel sets PKV_DEV_TIMEOUT in the device status word
+ * (read and cleared by pkv_get_device_status) and returns; the CUDA context
+ * stays usable. limit_us must lie in [1, 1000000], else PKV_E_SHAPE and nothing
+ * is launched; PKV_E_CUDA if the launch fails. */
+int pkv_selftest_bounded_wait(int32_t limit_us, pkv_stream_t stream);
+
 /* Library version string. */
 const char* pkv_version(void);
 

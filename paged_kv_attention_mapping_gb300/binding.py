@@ -28,6 +28,7 @@ EXPORTED = (
     "pkv_paged_attention_no_alloc",
     "pkv_status_string",
     "pkv_get_device_status",
+    "pkv_selftest_bounded_wait",
     "pkv_set_kernel_timing",
     "pkv_kernel_times",
     "pkv_version",
@@ -93,6 +94,8 @@ def lib():
     L.pkv_status_string.restype = ctypes.c_char_p
     L.pkv_get_device_status.argtypes = [P32, vp]
     L.pkv_get_device_status.restype = ctypes.c_int
+    L.pkv_selftest_bounded_wait.argtypes = [i32, vp]
+    L.pkv_selftest_bounded_wait.restype = ctypes.c_int
     L.pkv_set_kernel_timing.argtypes = [ctypes.c_int]
     L.pkv_set_kernel_timing.restype = ctypes.c_int
     L.pkv_kernel_times.argtypes = [ctypes.POINTER(ctypes.c_char_p), P32, ctypes.POINTER(ctypes.c_double), i32]
@@ -410,6 +413,12 @@ def rope_kv_append(q, k, v, positions, cos_sin, slot_mapping, k_cache, v_cache, 
                                   _ptr(v_cache), ctypes.byref(desc), _ptr(q_out), _stream_ptr(stream))
     _check(st, "pkv_rope_kv_append")
     return q_out
+
+
+def selftest_bounded_wait(limit_us: int, stream=None) -> None:
+    """Enqueue the failure-path self-test (pkv_selftest_bounded_wait): a wait
+    that nothing completes gives up after ~limit_us and sets PKV_DEV_TIMEOUT."""
+    _check(lib().pkv_selftest_bounded_wait(int(limit_us), _stream_ptr(stream)), "pkv_selftest_bounded_wait")
 
 
 def device_status(stream=None) -> int:

@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 SOURCES = ["pkv_api.cu", "pkv_append.cu", "pkv_plan.cu", "pkv_rows.cu", "pkv_prefill_tc.cu", "pkv_pack.cpp",
            "pkv_no_alloc.cu", "pkv_decode.cu", "pkv_tma.cu",
-           "pkv_prefill_tc2.cu", "pkv_pool.cpp", "pkv_rope.cu"]
+           "pkv_prefill_tc2.cu", "pkv_pool.cpp", "pkv_rope.cu", "pkv_selftest.cu"]
 
 
 def nvcc():

@@ -1,0 +1,46 @@
+"""Failure detection on the GPU without a fault: a kernel wait that nothing
+completes gives up after its limit, the device status word reports
+PKV_DEV_TIMEOUT, and the context keeps running ticks."""
+import time
+
+import pytest
+import torch
+
+from paged_kv_attention_mapping_gb300 import binding
+from paged_kv_attention_mapping_gb300 import workloads as W
+
+from test_gpu_parity import run_and_compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    return d
+
+
+def test_bounded_wait_gives_up_and_reports(dev):
+    assert binding.device_status() == 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    binding.selftest_bounded_wait(20000)          # 20 ms
+    st = binding.device_status()                  # waits for the stream
+    dt = time.perf_counter() - t0
+    assert st == binding.DEV_TIMEOUT
+    assert dt >= 0.015, dt
+    # the status was read and cleared; the context still runs a tick exactly
+    assert binding.device_status() == 0
+    w = W.random_workload(41, 4, 8, 2, 64, 16, "bf16", (1, 70), 200)
+    run_and_compare(w, dev)
+    assert binding.device_status() == 0
+
+
+def test_bounded_wait_rejects_limits_outside_its_range(dev):
+    for bad in (0, -5, 1000001):
+        with pytest.raises(RuntimeError):
+            binding.selftest_bounded_wait(bad)
+    assert binding.device_status() == 0
