@@ -91,6 +91,15 @@ def tick_work(w, kv_elt=None):
     dec_rows = [r for r in w.requests if r.q_len == 1]
     chunk = [r for r in w.requests if r.q_len > 1]
     decode_kv = sum(2 * r.kv_len * row_bytes for r in dec_rows)
+    # unique K/V bytes of the decode rows: a page shared by several page tables
+    # (a common prefix) holds its slots once in HBM, however many rows read it
+    slots_read = {}
+    for r in dec_rows:
+        for n, page in enumerate(r.pages):
+            used = min(s.page_size, r.kv_len - n * s.page_size)
+            if used > 0 and used > slots_read.get(page, 0):
+                slots_read[page] = used
+    decode_kv_unique = sum(2 * n * row_bytes for n in slots_read.values())
     decode_qo = sum(2 * s.num_q_heads * s.head_dim * elt + 4 * s.num_q_heads for r in dec_rows)
     decode_pt = sum(4 * len(r.pages) for r in dec_rows)
     pairs = sum(r.q_len * (r.kv_len - r.q_len) + r.q_len * (r.q_len + 1) // 2 for r in chunk)
@@ -101,6 +110,7 @@ def tick_work(w, kv_elt=None):
     q_bytes = w.total_q * s.num_q_heads * s.head_dim * elt
     rope_append_bytes = append_bytes + 2 * q_bytes + 4 * w.total_q + 8 * w.total_q  # + Q read/write, positions, slots
     return dict(decode_bytes=decode_kv + decode_qo + decode_pt, decode_kv_bytes=decode_kv,
+                decode_unique_bytes=decode_kv_unique + decode_qo + decode_pt,
                 prefill_flops=prefill_flops, prefill_bytes=prefill_bytes, append_bytes=append_bytes,
                 rope_append_bytes=rope_append_bytes)
 
@@ -120,9 +130,30 @@ def kernel_roofline(kernel, ktimes, work, peaks, workload):
     nbytes = {"kv_append": work["append_bytes"], "kv_append_quant": work["append_bytes"],
               "rope_append": work["rope_append_bytes"]}.get(kernel, work["decode_bytes"])
     ach = nbytes / avg_s / 1e9
-    return {"kernel": kernel, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": ach / peaks["hbm_gbs"], "traffic": traffic, "algorithmic_per_launch": nbytes,
-            "avg_launch_us": avg_s * 1e6, "peak_source": peaks["source"] + " copy bandwidth"}
+    res = {"kernel": kernel, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+           "frac": ach / peaks["hbm_gbs"], "traffic": traffic, "algorithmic_per_launch": nbytes,
+           "avg_launch_us": avg_s * 1e6, "peak_source": peaks["source"] + " copy bandwidth"}
+    if kernel in ("decode", "rows") and work["decode_unique_bytes"] < work["decode_bytes"]:
+        # pages shared by several rows: the bytes HBM must deliver at least once
+        ach_u = work["decode_unique_bytes"] / avg_s / 1e9
+        res.update(algorithmic_unique_per_launch=work["decode_unique_bytes"], achieved_unique=ach_u,
+                   frac_unique=ach_u / peaks["hbm_gbs"])
+    return res
+
+
+def tick_roofline(work, peaks, ms_per_step):
+    """Bounds of the whole step against its measured time: every byte the step
+    must move at the copy bandwidth plus every flop at the bf16 peak, one after
+    the other (serial) or fully overlapped (memory-bound and tensor-bound work
+    on disjoint SMs at once, the larger of the two)."""
+    nbytes = work["decode_bytes"] + work["append_bytes"] + work["prefill_bytes"]
+    t_mem = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_flop = work["prefill_flops"] / (peaks["bf16_tflops"] * 1e12)
+    t = ms_per_step / 1000.0
+    return {"bytes": nbytes, "flops": work["prefill_flops"], "t_mem_us": t_mem * 1e6, "t_flop_us": t_flop * 1e6,
+            "t_serial_us": (t_mem + t_flop) * 1e6, "t_overlap_us": max(t_mem, t_flop) * 1e6,
+            "measured_us": t * 1e6, "frac_serial": (t_mem + t_flop) / t, "frac_overlap": max(t_mem, t_flop) / t,
+            "peak_source": peaks["source"] + " copy bandwidth and bf16 burst"}
 
 
 # ---------------------------------------------------------------------------
@@ -185,9 +216,26 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU oracle on a bounded sample (the reported baseline)
 
+def host_threads():
+    """(host cores this process may run on, BLAS threads the oracle's NumPy uses)."""
+    cores = len(os.sched_getaffinity(0))
+    blas = None
+    try:
+        from threadpoolctl import threadpool_info
+        blas = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        env = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+        blas = int(env) if env else None
+    return cores, blas
+
+
 def oracle_sample(w, seconds=12.0, seed=0):
-    """Time the oracle (pack, append, attend) on a sample of the tick's rows and
-    scale to the whole tick: returns (tokens/s, description, threads)."""
+    """Time the oracle (pack, append, attend) on a sample of the tick's rows
+    drawn in the tick's own proportion of decode rows to chunk rows (chunk rows
+    uniformly over each chunk, up to 64 per draw). Returns a dict: rows and
+    oracle seconds of the sample, the sample's rows per second (the oracle's
+    throughput on this workload) and a description. Only the oracle calls are
+    timed, not the drawing of the inputs."""
     import oracle
     vals_rng = np.random.default_rng([w.seed, 7])
     s = w.shape
@@ -207,10 +255,11 @@ def oracle_sample(w, seconds=12.0, seed=0):
     done = {"decode": 0, "chunk": 0}
     wall_deadline = time.perf_counter() + 3 * seconds   # the value draws take time too
     while sum(spent.values()) < seconds and time.perf_counter() < wall_deadline:
-        kind = min((k for k in kinds if kinds[k]), key=lambda k: spent[k] / max(rows_total[k], 1) if done[k] else -1)
+        # the kind furthest behind its share of the tick's rows
+        kind = min((k for k in kinds if kinds[k]), key=lambda k: done[k] / rows_total[k])
         b = int(rng.choice(kinds[kind]))
         r = w.requests[p["order"][b]]
-        n_rows = r.q_len if kind == "decode" else min(16, r.q_len)
+        n_rows = r.q_len if kind == "decode" else min(64, r.q_len)
         # this sequence's pages, a fresh draw of its values, its new tokens
         pages = list(range(len(r.pages)))
         kc = W.round_to_dtype(vals_rng.standard_normal((len(pages), s.page_size, s.num_kv_heads, s.head_dim),
@@ -228,17 +277,20 @@ def oracle_sample(w, seconds=12.0, seed=0):
         oracle.paged_attention(qn, sp["cu_seqlens_q"], sp["kv_lens"], sp["page_tables"], kc2, vc2, w.scale, rows=rows)
         spent[kind] += time.perf_counter() - t0
         done[kind] += n_rows
-    est = t_pack + sum(spent[k] / done[k] * rows_total[k] for k in kinds if rows_total[k])
-    tokens_s = w.total_q / est
-    desc = (f"oracle on {done['decode']} decode rows and {done['chunk']} chunk rows drawn from the tick "
-            f"({sum(spent.values()):.1f} s of CPU), scaled per row kind to all {w.total_q} rows")
-    threads = 1
-    try:
-        from threadpoolctl import threadpool_info
-        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
-    except Exception:
-        threads = int(os.environ.get("OMP_NUM_THREADS", "0") or 0) or len(os.sched_getaffinity(0))
-    return tokens_s, desc, threads
+    rows = sum(done.values())
+    secs = t_pack * rows / w.total_q + sum(spent.values())   # the tick's packing, prorated to the sample
+    desc = (f"oracle on {done['decode']} decode rows and {done['chunk']} chunk rows drawn from the tick in its "
+            f"proportion of decode to chunk rows ({secs:.2f} s of CPU)")
+    return dict(rows=rows, seconds=secs, tokens_s=rows / secs, desc=desc)
+
+
+def bench_config(args, T, world):
+    """The config object both arms print (the same workload and protocol)."""
+    return {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"
+                        + (", RoPE fused into the append" if args.rope else "")
+                        + (", e4m3 KV cache (per-KV-head scales)" if args.kv_fp8 else ""),
+            "l2": "flushed between GPU steps (512 MB write, outside the step events)",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
 
 
 # ---------------------------------------------------------------------------
@@ -254,29 +306,36 @@ def dist_setup(n_gpus):
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on the host cores. Each
+    step is one bounded sample of the workload's rows (oracle_sample); `value`
+    is the rows the timed steps processed over their oracle seconds."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     w = W.make_workload(args.workload)
-    per_step = []
-    desc = ""
-    threads = 1
-    total_budget = args.ref_seconds
     steps = max(1, args.steps)
-    secs = max(0.05, total_budget / (steps + args.warmup))   # oracle seconds per step
+    secs = max(0.05, args.ref_seconds / (steps + args.warmup))   # oracle seconds per step
+    rows = 0
+    spent = 0.0
+    desc = ""
     for i in range(args.warmup + steps):
-        tok_s, desc, threads = oracle_sample(w, seconds=secs, seed=i)
+        smp = oracle_sample(w, seconds=secs, seed=i)
         if i >= args.warmup:
-            per_step.append(w.total_q / tok_s * 1000.0)
-    ms = statistics.mean(per_step)
-    value = w.total_q / (ms / 1000.0)
+            rows += smp["rows"]
+            spent += smp["seconds"]
+            desc = smp["desc"]
+    value = rows / spent
+    ms = spent * 1000.0 / steps
+    cores, blas = host_threads()
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                             "sample": desc},
+            "config": bench_config(args, w.total_q, world),
+            "rows_per_step": rows / steps,
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas or cores, "host_cores": cores,
+                             "blas_threads": blas, "kind": "oracle",
+                             "sample": f"each step: {desc}; last step shown"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -527,20 +586,20 @@ def main():
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        tok_s, desc, threads = oracle_sample(w, seconds=args.cpu_seconds)
-        cpu = {"value": tok_s, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
+        smp = oracle_sample(w, seconds=args.cpu_seconds)
+        cores, blas = host_threads()
+        cpu = {"value": smp["tokens_s"], "unit": "tokens/s", "cores": blas or cores, "host_cores": cores,
+               "blas_threads": blas, "kind": "oracle", "sample": smp["desc"]}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": s.dtype + ("+e4m3 cache" if args.kv_fp8 else ""), "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"
-                               + (", RoPE fused into the append" if args.rope else "")
-                               + (", e4m3 KV cache (per-KV-head scales)" if args.kv_fp8 else ""),
-                   "tokens_per_step": T, "l2": "flushed between steps (512 MB write, outside the step events)",
-                   "launch": "CUDA graph replay of the step (eager launches reported under eager)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "config": bench_config(args, T, world),
+        "tokens_per_step": T,
+        "launch": "CUDA graph replay of the step (eager launches reported under eager)",
         "roofline": roof,
+        "roofline_tick": tick_roofline(work, peaks, ms),
         "roofline_decode": roof_decode,
         "roofline_append": roof_append,
         "decode_hbm_gbs": decode_gbs,

@@ -378,14 +378,22 @@ int pkv_set_kernel_timing(int enable);
 int pkv_kernel_times(const char** names, int32_t* launches, double* total_ms, int32_t max);
 
 /* Self-test of the failure path (the pages have no counterpart; it checks the
- * library's own error handling). Enqueues on `stream` one CTA whose thread
- * waits, with the bounded mbarrier wait that every kernel of the library uses,
- * on a barrier that nothing ever completes. After about limit_us microseconds
- * the wait gives up, the kernel sets PKV_DEV_TIMEOUT in the device status word
- * (read and cleared by pkv_get_device_status) and returns; the CUDA context
- * stays usable. limit_us must lie in [1, 1000000], else PKV_E_SHAPE and nothing
- * is launched; PKV_E_CUDA if the launch fails. */
-int pkv_selftest_bounded_wait(int32_t limit_us, pkv_stream_t stream);
+ * library's own error handling). Enqueues on `stream` one CTA laid out like
+ * the prefill kernel's (a producer warp, an MMA-issuer thread, eight softmax
+ * warps), each waiting, through the bounded pipeline wait that every decode and
+ * prefill kernel of the library uses, on a barrier that nothing ever completes.
+ * The producer warp waits with a limit of limit_us microseconds, gives up
+ * first, raises the CTA's abort flag and records PKV_DEV_TIMEOUT in the CTA's
+ * error word and in the device status word (read and cleared by
+ * pkv_get_device_status); the other warps see the flag and return. The CUDA
+ * context stays usable.
+ *  - result: device int32[2] or NULL. [0] = the CTA's error word
+ *    (PKV_DEV_TIMEOUT), [1] = warps that left their wait without the barrier
+ *    (10 when every warp drained). Cleared on `stream` before the launch.
+ *  - limit_us must lie in [1, 1000000], else PKV_E_SHAPE and nothing is
+ *    launched; PKV_E_ALIGN if result is not 4-byte aligned; PKV_E_CUDA if the
+ *    launch fails. */
+int pkv_selftest_bounded_wait(int32_t limit_us, int32_t* result, pkv_stream_t stream);
 
 /* Library version string. */
 const char* pkv_version(void);

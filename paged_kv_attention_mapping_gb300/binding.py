@@ -94,7 +94,7 @@ def lib():
     L.pkv_status_string.restype = ctypes.c_char_p
     L.pkv_get_device_status.argtypes = [P32, vp]
     L.pkv_get_device_status.restype = ctypes.c_int
-    L.pkv_selftest_bounded_wait.argtypes = [i32, vp]
+    L.pkv_selftest_bounded_wait.argtypes = [i32, vp, vp]
     L.pkv_selftest_bounded_wait.restype = ctypes.c_int
     L.pkv_set_kernel_timing.argtypes = [ctypes.c_int]
     L.pkv_set_kernel_timing.restype = ctypes.c_int
@@ -278,6 +278,35 @@ def alloc_workspace(num_seqs, total_q, num_q_heads, k_cache, max_kv_len):
     return torch.empty(n, dtype=torch.uint8, device=k_cache.device)
 
 
+def _check_attention_args(where, q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_cache, out, lse,
+                          extra=(), q_matches_cache=True):
+    """The checks every attention call makes before any pointer reaches the
+    library: CUDA, contiguous, int32 index tensors, consistent dtypes and shapes."""
+    import torch
+    for t in (cu_seqlens_q, kv_lens, page_tables):
+        if t.dtype != torch.int32:
+            raise TypeError(f"{where}: index tensors must be int32")
+    if v_cache.dtype != k_cache.dtype or v_cache.shape != k_cache.shape:
+        raise TypeError(f"{where}: k_cache and v_cache must share one dtype and shape")
+    if q_matches_cache and q.dtype != k_cache.dtype:
+        raise TypeError(f"{where}: q, k_cache and v_cache must share one dtype")
+    for t in (q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_cache) + tuple(extra):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{where} needs contiguous CUDA tensors")
+    if q.dim() != 3 or page_tables.dim() != 2 or cu_seqlens_q.dim() != 1 or kv_lens.dim() != 1:
+        raise ValueError(f"{where}: q [T, Hq, d], cu_seqlens_q [B+1], kv_lens [B], page_tables [B, W]")
+    B = int(cu_seqlens_q.shape[0]) - 1
+    if B < 0 or int(kv_lens.shape[0]) < B or int(page_tables.shape[0]) < B:
+        raise ValueError(f"{where}: cu_seqlens_q, kv_lens and page_tables disagree on the number of sequences")
+    if out is not None:
+        if not out.is_cuda or not out.is_contiguous() or out.dtype != q.dtype or out.shape != q.shape:
+            raise ValueError(f"{where}: out must be a contiguous CUDA tensor shaped and typed like q")
+    if lse is not None:
+        if (not lse.is_cuda or not lse.is_contiguous() or lse.dtype != torch.float32
+                or tuple(lse.shape) != tuple(q.shape[:2])):
+            raise ValueError(f"{where}: lse must be a contiguous float32 CUDA tensor [T, Hq]")
+
+
 def paged_attention(q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_cache, scale: float, max_kv_len: int,
                     out=None, lse=None, workspace=None, want_lse: bool = True, stream=None):
     """Attention of packed query rows over their pages (pkv_paged_attention).
@@ -285,27 +314,22 @@ def paged_attention(q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_cache, sca
     q [T, Hq, d] (cache dtype); cu_seqlens_q int32 [B+1]; kv_lens int32 [B];
     page_tables int32 [B, W]; caches [N, P, Hkv, d]. Returns (out, lse)."""
     import torch
+    _check_attention_args("paged_attention", q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_cache, out, lse)
     T, Hq, D = q.shape
     B = int(cu_seqlens_q.shape[0]) - 1
-    for t in (q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_cache):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("paged_attention needs contiguous CUDA tensors")
-    for t in (cu_seqlens_q, kv_lens, page_tables):
-        if t.dtype != torch.int32:
-            raise TypeError("index tensors must be int32")
-    if q.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
-        raise TypeError("q, k_cache and v_cache must share one dtype")
     if out is None:
         out = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = alloc_workspace(B, T, Hq, k_cache, max_kv_len)
+    elif not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("paged_attention: workspace must be a contiguous CUDA tensor")
     desc = cache_desc(k_cache)
     st = lib().pkv_paged_attention(_ptr(q), _ptr(cu_seqlens_q), _ptr(kv_lens), _ptr(page_tables), B, int(T), int(Hq),
                                    int(page_tables.shape[1]), int(max_kv_len), _ptr(k_cache), _ptr(v_cache),
                                    ctypes.byref(desc), ctypes.c_float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
-                                   int(workspace.numel()), _stream_ptr(stream))
+                                   int(workspace.numel() * workspace.element_size()), _stream_ptr(stream))
     _check(st, "pkv_paged_attention")
     return out, lse
 
@@ -314,8 +338,12 @@ def paged_attention_no_alloc(q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_c
                              max_kv_len: int, out=None, lse=None, want_lse: bool = True, stream=None):
     """pkv_paged_attention_no_alloc: as paged_attention, but the library uses its
     own fixed device scratch array instead of a caller workspace (for callers
-    that cannot allocate device memory). Output buffers may still be passed in."""
+    that cannot allocate device memory). Output buffers may still be passed in;
+    when they are not, this wrapper allocates them with torch (the C call
+    itself never allocates)."""
     import torch
+    _check_attention_args("paged_attention_no_alloc", q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_cache,
+                          out, lse)
     T, Hq, D = q.shape
     B = int(cu_seqlens_q.shape[0]) - 1
     if out is None:
@@ -353,26 +381,27 @@ def paged_attention_fp8(q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_cache,
     """Attention over an fp8 e4m3 cache (pkv_paged_attention_fp8): q/out bf16 or
     f16 [T, Hq, d]; caches uint8 codes [N, P, Hkv, d]; element = code * scale[head]."""
     import torch
+    _check_attention_args("paged_attention_fp8", q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_cache, out, lse,
+                          extra=(k_scale, v_scale), q_matches_cache=False)
+    if k_scale.dtype != torch.float32 or v_scale.dtype != torch.float32:
+        raise TypeError("paged_attention_fp8: scales must be float32")
     T, Hq, D = q.shape
     B = int(cu_seqlens_q.shape[0]) - 1
-    for t in (q, cu_seqlens_q, kv_lens, page_tables, k_cache, v_cache, k_scale, v_scale):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("paged_attention_fp8 needs contiguous CUDA tensors")
-    for t in (cu_seqlens_q, kv_lens, page_tables):
-        if t.dtype != torch.int32:
-            raise TypeError("index tensors must be int32")
     if out is None:
         out = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = alloc_workspace(B, T, Hq, k_cache, max_kv_len)
+    elif not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("paged_attention_fp8: workspace must be a contiguous CUDA tensor")
     desc = cache_desc(k_cache)
     st = lib().pkv_paged_attention_fp8(_ptr(q), _dtype_code(q), _ptr(cu_seqlens_q), _ptr(kv_lens),
                                        _ptr(page_tables), B, int(T), int(Hq), int(page_tables.shape[1]),
                                        int(max_kv_len), _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),
                                        _ptr(k_scale), _ptr(v_scale), ctypes.c_float(scale), _ptr(out), _ptr(lse),
-                                       _ptr(workspace), int(workspace.numel()), _stream_ptr(stream))
+                                       _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                                       _stream_ptr(stream))
     _check(st, "pkv_paged_attention_fp8")
     return out, lse
 
@@ -415,10 +444,18 @@ def rope_kv_append(q, k, v, positions, cos_sin, slot_mapping, k_cache, v_cache, 
     return q_out
 
 
-def selftest_bounded_wait(limit_us: int, stream=None) -> None:
-    """Enqueue the failure-path self-test (pkv_selftest_bounded_wait): a wait
-    that nothing completes gives up after ~limit_us and sets PKV_DEV_TIMEOUT."""
-    _check(lib().pkv_selftest_bounded_wait(int(limit_us), _stream_ptr(stream)), "pkv_selftest_bounded_wait")
+def selftest_bounded_wait(limit_us: int, result=None, stream=None) -> None:
+    """Enqueue the failure-path self-test (pkv_selftest_bounded_wait): a CTA laid
+    out like the prefill kernel's waits on barriers that nothing completes; the
+    producer warp gives up after ~limit_us and sets PKV_DEV_TIMEOUT, the other
+    warps drain through the abort flag. `result`: optional device int32 [2]
+    tensor (error word, warps that returned)."""
+    if result is not None:
+        import torch
+        if not result.is_cuda or result.dtype != torch.int32 or result.numel() < 2 or not result.is_contiguous():
+            raise ValueError("selftest_bounded_wait: result must be a contiguous int32 CUDA tensor of 2 entries")
+    _check(lib().pkv_selftest_bounded_wait(int(limit_us), _ptr(result), _stream_ptr(stream)),
+           "pkv_selftest_bounded_wait")
 
 
 def device_status(stream=None) -> int:

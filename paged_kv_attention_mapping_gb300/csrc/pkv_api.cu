@@ -158,7 +158,8 @@ extern "C" int pkv_kv_append(const void* k, const void* v, const int64_t* slot_m
   const DeviceFacts* f = device_facts();
   if (!f) return PKV_E_CUDA;
   if (!f->ok) return PKV_E_DEVICE;
-  cudaError_t e = launch_append(k, v, slot_mapping, num_tokens, k_cache, v_cache, *cache, (cudaStream_t)stream);
+  cudaError_t e = launch_append(k, v, slot_mapping, num_tokens, k_cache, v_cache, *cache, f->num_sms,
+                                (cudaStream_t)stream);
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "kv_append");
 }
 
@@ -182,7 +183,7 @@ extern "C" int pkv_rope_kv_append(const void* q, const void* k, const void* v, c
   if (!f) return PKV_E_CUDA;
   if (!f->ok) return PKV_E_DEVICE;
   cudaError_t e = launch_rope_append(q, k, v, positions, cos_sin, max_pos, slot_mapping, num_tokens, num_q_heads,
-                                     k_cache, v_cache, q_out, *cache, f->status, (cudaStream_t)stream);
+                                     k_cache, v_cache, q_out, *cache, f->status, f->num_sms, (cudaStream_t)stream);
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "rope_append");
 }
 
@@ -200,14 +201,37 @@ extern "C" size_t pkv_paged_attention_workspace_size(int32_t num_seqs, int32_t t
 // prefill kernel (when the shape has one); shorter ones go row by row.
 static constexpr int TC_MIN_Q = 64;
 
+// Shrink the partial-result room of `lay` so that the whole layout fits
+// `bytes` (the plan's per-row arrays keep their sizes). The planner then widens
+// the split until the partials fit, which changes only how keys are split, not
+// what is computed. Returns false when not even one partial fits.
+static bool fit_partials(PlanLayout* lay, int32_t g, int32_t head_dim, size_t bytes) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t per_part = (size_t)g * 4 + (size_t)g * head_dim * 4;   // lse + o of one partial
+  const size_t base = lay->part_lse;
+  if (base + 1024 > bytes) return false;
+  size_t cap = (bytes - base - 512) / per_part;
+  if (cap > (size_t)lay->partial_cap) cap = (size_t)lay->partial_cap;
+  if (cap < 1) return false;
+  lay->partial_cap = (int32_t)cap;
+  lay->part_o = base + al(cap * (size_t)g * 4);
+  lay->total = lay->part_o + al(cap * (size_t)g * head_dim * 4);
+  return lay->total <= bytes;
+}
+
 // Shared body of the attention entry points: host checks, the device plan,
 // then the kernels on `stream`. q_dtype is the q/out element type; an fp8
 // cache (cache->dtype == PKV_FP8_E4M3) comes with its per-KV-head scales.
-static int attention_impl(const void* q, int q_dtype, const int32_t* cu_seqlens_q, const int32_t* kv_lens,
-                          const int32_t* page_tables, int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
-                          int32_t max_pages_per_seq, int32_t max_kv_len, const void* k_cache, const void* v_cache,
-                          const pkv_cache_desc* cache, const float* k_scale, const float* v_scale, float scale,
-                          void* out, float* lse, void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+// With `scratch` the workspace is the fixed-size area that scratch() returns
+// (looked up only after the host checks pass), and its partial-result room is
+// fitted to workspace_bytes (fit_partials) instead of the area having to hold
+// the standard layout.
+int pkv::attention_impl(const void* q, int q_dtype, const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                        const int32_t* page_tables, int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                        int32_t max_pages_per_seq, int32_t max_kv_len, const void* k_cache, const void* v_cache,
+                        const pkv_cache_desc* cache, const float* k_scale, const float* v_scale, float scale,
+                        void* out, float* lse, void* workspace, size_t workspace_bytes, ScratchFn scratch,
+                        pkv_stream_t stream) {
   int st = check_cache(cache);
   if (st != PKV_OK) return st;
   const bool fp8 = cache->dtype == PKV_FP8_E4M3;
@@ -219,18 +243,24 @@ static int attention_impl(const void* q, int q_dtype, const int32_t* cu_seqlens_
   if (total_q > 0 && max_pages_per_seq < 1) return PKV_E_SHAPE;
   if ((int64_t)max_pages_per_seq * cache->page_size > INT32_MAX) return PKV_E_SHAPE;
   if (total_q == 0) return PKV_OK;
-  if (!q || !cu_seqlens_q || !kv_lens || !page_tables || !k_cache || !v_cache || !out || !workspace)
+  if (!q || !cu_seqlens_q || !kv_lens || !page_tables || !k_cache || !v_cache || !out || (!workspace && !scratch))
     return PKV_E_NULL;
   if (fp8 && (!k_scale || !v_scale)) return PKV_E_NULL;
   if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) || ((uintptr_t)lse & 3u))
     return PKV_E_ALIGN;
   if (((uintptr_t)workspace & 255u) != 0) return PKV_E_WORKSPACE;
-  const PlanLayout lay =
-      plan_layout(num_seqs, total_q, num_q_heads, cache->num_kv_heads, cache->head_dim, max_kv_len);
+  PlanLayout lay = plan_layout(num_seqs, total_q, num_q_heads, cache->num_kv_heads, cache->head_dim, max_kv_len);
+  if (scratch && !fit_partials(&lay, num_q_heads / cache->num_kv_heads, cache->head_dim, workspace_bytes))
+    return PKV_E_WORKSPACE;
   if (workspace_bytes < lay.total) return PKV_E_WORKSPACE;
   const DeviceFacts* f = device_facts();
   if (!f) return PKV_E_CUDA;
   if (!f->ok) return PKV_E_DEVICE;
+  if (scratch) {
+    workspace = scratch();
+    if (!workspace) return cuda_fail(cudaGetLastError(), "scratch address");
+    if (((uintptr_t)workspace & 255u) != 0) return PKV_E_WORKSPACE;
+  }
   cudaStream_t s = (cudaStream_t)stream;
 
   // fp8 caches have no tensor-core prefill kernel yet: their chunk rows take the row path.
@@ -318,7 +348,7 @@ extern "C" int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, c
   if (cache && cache->dtype == PKV_FP8_E4M3) return PKV_E_DTYPE;  // fp8 caches: pkv_paged_attention_fp8
   return attention_impl(q, cache ? cache->dtype : 0, cu_seqlens_q, kv_lens, page_tables, num_seqs, total_q,
                         num_q_heads, max_pages_per_seq, max_kv_len, k_cache, v_cache, cache, nullptr, nullptr, scale,
-                        out, lse, workspace, workspace_bytes, stream);
+                        out, lse, workspace, workspace_bytes, nullptr, stream);
 }
 
 extern "C" int pkv_paged_attention_fp8(const void* q, int32_t q_dtype, const int32_t* cu_seqlens_q,
@@ -332,7 +362,7 @@ extern "C" int pkv_paged_attention_fp8(const void* q, int32_t q_dtype, const int
   if (cache->dtype != PKV_FP8_E4M3 || (q_dtype != PKV_BF16 && q_dtype != PKV_F16)) return PKV_E_DTYPE;
   return attention_impl(q, q_dtype, cu_seqlens_q, kv_lens, page_tables, num_seqs, total_q, num_q_heads,
                         max_pages_per_seq, max_kv_len, k_cache, v_cache, cache, k_scale, v_scale, scale, out, lse,
-                        workspace, workspace_bytes, stream);
+                        workspace, workspace_bytes, nullptr, stream);
 }
 
 extern "C" int pkv_kv_append_quant(const void* k, const void* v, int32_t src_dtype, const int64_t* slot_mapping,
@@ -350,7 +380,7 @@ extern "C" int pkv_kv_append_quant(const void* k, const void* v, int32_t src_dty
   if (!f) return PKV_E_CUDA;
   if (!f->ok) return PKV_E_DEVICE;
   cudaError_t e = launch_append_quant(k, v, src_dtype, slot_mapping, num_tokens, k_cache, v_cache, *cache, k_scale,
-                                      v_scale, f->status, (cudaStream_t)stream);
+                                      v_scale, f->status, f->num_sms, (cudaStream_t)stream);
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "kv_append_quant");
 }
 

@@ -6,20 +6,31 @@
 // are read through the page table, never gathered into a dense copy.
 //
 // Work item = (row, KV head, split of the keys), from the device plan. One
-// CTA = 1 producer warp + 4 compute warps, two CTAs per SM, persistent:
-//  * producer: takes items from the plan (atomic counter) into a 2-deep item
-//    queue and streams each item's 64-key K and V tiles out of the page pool
-//    with TMA (128-byte swizzled boxes, one per page or 64-key run) into a
-//    3-stage shared-memory ring; it runs ahead across item boundaries.
-//  * compute warps: warp w owns keys 16w..16w+15 of every tile. QK: two lanes
-//    per key (each half of head_dim), q of all g heads broadcast from shared
-//    memory, packed fp32x2 FMAs, one shuffle to join the halves. Online softmax
-//    per warp (exp2 domain, shuffle reductions over the warp's keys). PV: lanes
-//    own head_dim/32 dims for all g heads, p broadcast by shuffle.
-//  * end of item: the 4 warps' (m, l, o) merge in shared memory; the result
-//    goes to out/lse, or to the workspace as a partial when the row was split.
-// Keys past the item's end are masked in QK and skipped in PV, so stale or NaN
-// slots never enter a sum. Every mbarrier wait is bounded (PKV_DEV_TIMEOUT).
+// CTA = 1 producer warp + 4 compute warps, persistent, 2 CTAs per SM (3 when a
+// stage is at most 16 KB, i.e. head_dim 64 at 16 bits or fp8 with groups up to 8):
+//  * producer: takes items from the plan (CTA c starts with item c when the
+//    whole grid starts at once, then an atomic counter) into a 2-slot item
+//    queue, decoding each with warp-wide searches of the plan; bulk-copies the
+//    item's q rows; holds 32 logical pages of the page table in its lanes; and
+//    streams 64-key K and V tiles with 3-D TMA boxes (one per page, K or V and
+//    128-byte swizzle atom, issued by that many lanes at once) into a ring of
+//    3-6 stages, running ahead across item boundaries.
+//  * compute warps: warp w owns keys 16w..16w+15 of every tile. 16-bit and
+//    fp8 caches use mma.sync m16n8k16 with fp32 accumulators. For groups up to
+//    8 the keys are the M rows: S^T = K Q^T and O^T += V^T P^T with the group's
+//    heads as the 8 N columns, K and V fragments from ldmatrix (.trans for V),
+//    P^T transposed in registers with movmatrix; groups of 16 put the heads on
+//    the M rows instead. fp8 codes are widened to fp16 in registers, the K scale
+//    folded into the score scale and the V scale into the result. fp32 caches
+//    run on CUDA cores with packed fp32x2 FMAs. Online softmax in the exp2
+//    domain with shuffle reductions.
+//  * end of item: the 4 warps' (m, l, o) merge in shared memory (in the stage
+//    of the item's last tile where a separate buffer would cost a CTA per SM);
+//    the result goes to out/lse, or to the workspace as a partial when the row
+//    was split.
+// Keys past the item's end are masked in S and their V rows zeroed in shared
+// memory, so stale or NaN slots never enter a sum. Every pipeline wait is the
+// bounded sm100::wait_or_abort (PKV_DEV_TIMEOUT, then drain).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -100,24 +111,6 @@ __device__ __forceinline__ float2 cvt_pair<__nv_bfloat16>(uint32_t w) {
 template <>
 __device__ __forceinline__ float2 cvt_pair<__half>(uint32_t w) {
   return __half22float2(*reinterpret_cast<const __half2*>(&w));
-}
-
-__device__ __forceinline__ bool wait_flag(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* ctrl,
-                                          int32_t* dev_status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > 2000000000ull || it > (1u << 28)) {
-        *abort_flag = 1;
-        atomicOr(&ctrl[CTRL_ERR], PKV_DEV_TIMEOUT);
-        atomicOr(dev_status, PKV_DEV_TIMEOUT);
-        return false;
-      }
-    }
-  }
 }
 
 // First index i in [0, n) with a[i] > x (n if none) for a non-decreasing a,
@@ -301,8 +294,7 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
     uint32_t q_loads = 0;   // q copies issued (lane 0), slots alternate from 0
     for (uint32_t it = 0;; ++it) {
       const int slot = it & 1;
-      if (!__all_sync(0xffffffffu, wait_flag(&bar_iempty[slot], ((it >> 1) & 1) ^ 1, &s_abort, p.ctrl,
-                                             p.dev_status)))
+      if (!warp_wait_or_abort(&bar_iempty[slot], ((it >> 1) & 1) ^ 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status))
         break;
       // next item, decoded by the whole warp (few dependent loads)
       // When every CTA starts at once (not beside the prefill kernel, whose SMs
@@ -377,7 +369,7 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
         }
         const uint32_t st = stage_use % C::NST, round = stage_use / C::NST;
         ++stage_use;
-        if (!__all_sync(0xffffffffu, wait_flag(&bar_empty[st], (round & 1) ^ 1, &s_abort, p.ctrl, p.dev_status))) {
+        if (!warp_wait_or_abort(&bar_empty[st], (round & 1) ^ 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
           ok = false;
           break;
         }
@@ -433,7 +425,7 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
   // barrier of the 128 compute threads, bounded like every other wait
   auto cw_sync = [&]() -> bool {
     mbar_arrive(&bar_cw);
-    const bool ok = wait_flag(&bar_cw, cw_phase & 1, &s_abort, p.ctrl, p.dev_status);
+    const bool ok = wait_or_abort(&bar_cw, cw_phase & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status);
     ++cw_phase;
     return __all_sync(0xffffffffu, ok);
   };
@@ -453,7 +445,7 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
   const int grp = lane >> 2, tig = lane & 3;   // mma fragment coordinates
   for (uint32_t it = 0;; ++it) {
     const int slot = it & 1;
-    if (!__all_sync(0xffffffffu, wait_flag(&bar_ifull[slot], (it >> 1) & 1, &s_abort, p.ctrl, p.dev_status))) break;
+    if (!warp_wait_or_abort(&bar_ifull[slot], (it >> 1) & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) break;
     const Item item = s_item[slot];
     if (!item.valid) break;
     const T* qg = (const T*)p.q + ((int64_t)item.r * p.Hq + item.kvh * G) * D;
@@ -471,7 +463,7 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
       // the contraction index of each 16-dim block is permuted so that k slots
       // (2tig, 2tig+1 | 2tig+8, 2tig+9) hold dims (4tig, 4tig+1 | 4tig+2, 4tig+3),
       // the four bytes one ldmatrix lane receives from a key row.
-      if (!__all_sync(0xffffffffu, wait_flag(&bar_q[slot], (it >> 1) & 1, &s_abort, p.ctrl, p.dev_status))) break;
+      if (!warp_wait_or_abort(&bar_q[slot], (it >> 1) & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) break;
       const T* qs = reinterpret_cast<const T*>(reinterpret_cast<const unsigned char*>(sQ) + slot * (G * D * 2));
       uint32_t qb[D / 16][2];
 #pragma unroll
@@ -499,7 +491,7 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
       for (int t = 0; t < item.n_tiles; ++t) {
         const uint32_t st = stage_use % C::NST, round = stage_use / C::NST;
         ++stage_use;
-        if (!__all_sync(0xffffffffu, wait_flag(&bar_full[st], round & 1, &s_abort, p.ctrl, p.dev_status))) {
+        if (!warp_wait_or_abort(&bar_full[st], round & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
           ok = false;
           break;
         }
@@ -669,7 +661,7 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
       for (int t = 0; t < item.n_tiles; ++t) {
         const uint32_t st = stage_use % C::NST, round = stage_use / C::NST;
         ++stage_use;
-        if (!__all_sync(0xffffffffu, wait_flag(&bar_full[st], round & 1, &s_abort, p.ctrl, p.dev_status))) {
+        if (!warp_wait_or_abort(&bar_full[st], round & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
           ok = false;
           break;
         }
@@ -849,7 +841,7 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
       for (int t = 0; t < item.n_tiles; ++t) {
         const uint32_t st = stage_use % C::NST, round = stage_use / C::NST;
         ++stage_use;
-        if (!__all_sync(0xffffffffu, wait_flag(&bar_full[st], round & 1, &s_abort, p.ctrl, p.dev_status))) {
+        if (!warp_wait_or_abort(&bar_full[st], round & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
           ok = false;
           break;
         }

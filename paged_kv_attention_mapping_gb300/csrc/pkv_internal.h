@@ -133,16 +133,34 @@ struct AttnArgs {
   bool after_prefill = false;      // the prefill kernel was launched just before (decode may overlap it)
 };
 
+// The append kernels' work split: token t has per_token 16-byte items; block b
+// takes tokens [b * tpb, (b + 1) * tpb) and its 256 threads take the items of
+// that span in order, so consecutive threads touch consecutive 16-byte vectors
+// of one token's rows (coalesced reads and writes). tpb is chosen so that a
+// thread has at most about four items and the grid has at least two blocks per
+// SM when the tick has enough tokens.
+struct TokenSpan {
+  int32_t T, per_token, tpb;
+  int64_t blocks() const { return ((int64_t)T + tpb - 1) / tpb; }
+};
+inline TokenSpan token_span(int32_t T, int32_t per_token, int num_sms, int items_per_thread) {
+  int32_t tpb = (256 * items_per_thread) / per_token;
+  if (tpb < 1) tpb = 1;
+  const int32_t for_grid = T / (2 * (num_sms > 0 ? num_sms : 1));   // tokens per block with 2 blocks per SM
+  if (for_grid < tpb) tpb = for_grid < 1 ? 1 : for_grid;
+  return TokenSpan{T, per_token, tpb};
+}
+
 cudaError_t launch_append(const void* k, const void* v, const int64_t* slots, int32_t T, void* kc, void* vc,
-                          const pkv_cache_desc& c, cudaStream_t s);
+                          const pkv_cache_desc& c, int num_sms, cudaStream_t s);
 // e4m3 cache: codes of x / scale[kv head], sources of type src_dtype (f32/f16/bf16).
 cudaError_t launch_append_quant(const void* k, const void* v, int src_dtype, const int64_t* slots, int32_t T,
                                 void* kc, void* vc, const pkv_cache_desc& c, const float* k_scale,
-                                const float* v_scale, int32_t* dev_status, cudaStream_t s);
+                                const float* v_scale, int32_t* dev_status, int num_sms, cudaStream_t s);
 cudaError_t launch_rope_append(const void* q, const void* k, const void* v, const int32_t* positions,
                                const float* cos_sin, int32_t max_pos, const int64_t* slots, int32_t T,
                                int32_t Hq, void* kc, void* vc, void* q_out, const pkv_cache_desc& c,
-                               int32_t* dev_status, cudaStream_t s);
+                               int32_t* dev_status, int num_sms, cudaStream_t s);
 cudaError_t launch_rows(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const AttnArgs& a, cudaStream_t s);
 // Returns cudaErrorNotSupported when the shape has no tensor-core path.
@@ -161,5 +179,20 @@ bool make_map_boxed(CUtensorMap* m, const void* base, CUtensorMapDataType dt, in
 
 // workers of the row kernel (for the split policy)
 int rows_kernel_workers(int num_sms);
+
+// The one body behind every attention entry point (pkv_api.cu): host checks,
+// the device plan and the kernel launches on `stream`. q_dtype is the q/out
+// element type; an fp8 cache comes with its per-KV-head scales. With a
+// `scratch` function the workspace argument is ignored: after the host checks
+// pass, scratch() gives a fixed area of workspace_bytes (nullptr on a CUDA
+// error), whose partial-result room is fitted to that size (the split then
+// grows until the partials fit). Without it the workspace must hold the
+// standard layout of pkv_paged_attention_workspace_size.
+using ScratchFn = char* (*)();
+int attention_impl(const void* q, int q_dtype, const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                   const int32_t* page_tables, int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                   int32_t max_pages_per_seq, int32_t max_kv_len, const void* k_cache, const void* v_cache,
+                   const pkv_cache_desc* cache, const float* k_scale, const float* v_scale, float scale, void* out,
+                   float* lse, void* workspace, size_t workspace_bytes, ScratchFn scratch, pkv_stream_t stream);
 
 }  // namespace pkv

@@ -81,24 +81,6 @@ struct Cfg {
   static constexpr uint32_t SMEM = Q_BYTES + NSLOT * SLOT_BYTES + P_BYTES + 1024;
 };
 
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                              int32_t* ctrl, int32_t* dev_status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > 2000000000ull || it > (1u << 28)) {
-        *abort_flag = 1;
-        atomicOr(&ctrl[CTRL_ERR], PKV_DEV_TIMEOUT);
-        atomicOr(dev_status, PKV_DEV_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float a, float b);
 template <>
@@ -216,8 +198,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int kv = 0; kv < 2 && ok; ++kv) {
           const uint32_t slot = ring % NSLOT, round = ring / NSLOT;
           ++ring;
-          if (!__all_sync(0xffffffffu, wait_or_abort(&bar_empty[slot], (round & 1) ^ 1, &s_abort, p.ctrl,
-                                                     p.dev_status))) {
+          if (!warp_wait_or_abort(&bar_empty[slot], (round & 1) ^ 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
             ok = false;
             break;
           }
@@ -265,8 +246,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (kv == 1 && j == ti.n_kv - 1) {
             if (ti.zero_from < BN) {
               // the last V tile holds slots past kv_len: zero them before PV
-              if (!__all_sync(0xffffffffu, wait_or_abort(&bar_full[slot], round & 1, &s_abort, p.ctrl,
-                                                         p.dev_status))) {
+              if (!warp_wait_or_abort(&bar_full[slot], round & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
                 ok = false;
                 break;
               }
@@ -294,15 +274,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t id_qk = idesc_f16(BM, BN, BF16, false);
         const uint32_t id_pv = idesc_f16(BM, D, BF16, true);
         const uint32_t base = ring;
-        bool ok = wait_or_abort(&bar_q, tile_cnt & 1, &s_abort, p.ctrl, p.dev_status);
+        bool ok = wait_or_abort(&bar_q, tile_cnt & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status);
         tc_fence_after();
         auto issue_pv = [&](int jj) -> bool {
           const uint32_t iv = base + 2 * jj + 1;
           const uint32_t slot = iv % NSLOT, round = iv / NSLOT;
-          if (!wait_or_abort(&bar_full[slot], round & 1, &s_abort, p.ctrl, p.dev_status)) return false;
-          if (jj == ti.n_kv - 1 && !wait_or_abort(&bar_vfix, tile_cnt & 1, &s_abort, p.ctrl, p.dev_status))
+          if (!wait_or_abort(&bar_full[slot], round & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) return false;
+          if (jj == ti.n_kv - 1 && !wait_or_abort(&bar_vfix, tile_cnt & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status))
             return false;
-          if (!wait_or_abort(&bar_pfull, p_cnt & 1, &s_abort, p.ctrl, p.dev_status)) return false;
+          if (!wait_or_abort(&bar_pfull, p_cnt & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) return false;
           ++p_cnt;
           tc_fence_after();
           const uint32_t v_base = smem_u32(sRing + slot * C::SLOT_BYTES);
@@ -321,8 +301,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const uint32_t ik = base + 2 * j;
           const uint32_t slot = ik % NSLOT, round = ik / NSLOT;
           const uint32_t sb = s_cnt & 1, su = s_cnt >> 1;
-          ok = wait_or_abort(&bar_full[slot], round & 1, &s_abort, p.ctrl, p.dev_status) &&
-               wait_or_abort(&bar_sfree[sb], (su & 1) ^ 1, &s_abort, p.ctrl, p.dev_status);
+          ok = wait_or_abort(&bar_full[slot], round & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status) &&
+               wait_or_abort(&bar_sfree[sb], (su & 1) ^ 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status);
           if (!ok) break;
           ++s_cnt;
           tc_fence_after();
@@ -355,7 +335,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t sb = s_cnt & 1, su = s_cnt >> 1;
         ++s_cnt;
         // tcgen05.ld/st are warp-collective: every decision before one is warp-uniform
-        if (!__all_sync(0xffffffffu, wait_or_abort(&bar_sfull[sb], su & 1, &s_abort, p.ctrl, p.dev_status))) {
+        if (!warp_wait_or_abort(&bar_sfull[sb], su & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
           ok = false;
           break;
         }
@@ -390,7 +370,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float m_new = grow ? fmaxf(mt, m_run) : m_run;
         if (j > 0) {
           // PV_{j-1} must be finished before P is overwritten or O rescaled
-          if (!__all_sync(0xffffffffu, wait_or_abort(&bar_odone, o_cnt & 1, &s_abort, p.ctrl, p.dev_status))) {
+          if (!warp_wait_or_abort(&bar_odone, o_cnt & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
             ok = false;
             break;
           }
@@ -434,9 +414,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_before();
         mbar_arrive(&bar_pfull);
       }
-      if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(&bar_odone, o_cnt & 1, &s_abort, p.ctrl, p.dev_status));
+      if (ok) ok = warp_wait_or_abort(&bar_odone, o_cnt & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status);
       ++o_cnt;
-      if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(&bar_vfix, tile_cnt & 1, &s_abort, p.ctrl, p.dev_status));
+      if (ok) ok = warp_wait_or_abort(&bar_vfix, tile_cnt & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status);
       tc_fence_after();
       if (ok) {
         // the whole warp reads O; only rows of the chunk are stored

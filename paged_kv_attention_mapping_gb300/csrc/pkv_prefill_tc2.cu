@@ -91,24 +91,6 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
-__device__ __forceinline__ bool wait2(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* ctrl,
-                                      int32_t* dev_status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > 2000000000ull || it > (1u << 28)) {
-        *abort_flag = 1;
-        atomicOr(&ctrl[CTRL_ERR], PKV_DEV_TIMEOUT);
-        atomicOr(dev_status, PKV_DEV_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -201,7 +183,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint32_t e = t & 1;
       // entry e is free again once every consumer is done with tile t - 2
       if (t >= 2 &&
-          !__all_sync(0xffffffffu, wait2(&bar_tempty[e], ((t >> 1) - 1) & 1, &s_abort, p.ctrl, p.dev_status))) {
+          !warp_wait_or_abort(&bar_tempty[e], ((t >> 1) - 1) & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
         ok = false;
         break;
       }
@@ -236,7 +218,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!ti.valid) break;
       const int32_t* pt = p.page_tables + (int64_t)ti.b * p.max_pages;
       // Q of this tile replaces the previous tile's once its last QK MMA is done
-      if (t >= 1 && !__all_sync(0xffffffffu, wait2(&bar_qempty, (t - 1) & 1, &s_abort, p.ctrl, p.dev_status))) {
+      if (t >= 1 && !warp_wait_or_abort(&bar_qempty, (t - 1) & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
         ok = false;
         break;
       }
@@ -253,8 +235,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int kv = 0; kv < 2 && ok; ++kv) {
           const uint32_t slot = ring % NS, round = ring / NS;
           ++ring;
-          if (!__all_sync(0xffffffffu,
-                          wait2(&bar_empty[slot], (round & 1) ^ 1, &s_abort, p.ctrl, p.dev_status))) {
+          if (!warp_wait_or_abort(&bar_empty[slot], (round & 1) ^ 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
             ok = false;
             break;
           }
@@ -301,7 +282,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           fills[slot] += 1;
           if (kv == 1 && j == ti.n_kv - 1) {
             if (ti.zero_from < BN) {
-              if (!__all_sync(0xffffffffu, wait2(&bar_full[slot], round & 1, &s_abort, p.ctrl, p.dev_status))) {
+              if (!warp_wait_or_abort(&bar_full[slot], round & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
                 ok = false;
                 break;
               }
@@ -350,7 +331,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       bool ok = true;
       for (uint32_t t = 0; ok; ++t) {
         const uint32_t e = t & 1;
-        if (!wait2(&bar_tfull[e], (t >> 1) & 1, &s_abort, p.ctrl, p.dev_status)) break;
+        if (!wait_or_abort(&bar_tfull[e], (t >> 1) & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) break;
         const Tile2 ti = s_tile[e];
         if (!ti.valid) break;
         // K_j is the tile's load 2j and V_j load 2j + 1 of the ring
@@ -361,11 +342,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           vph ^= 1;
         }
         ring += 2 * ti.n_kv;
-        ok = wait2(&bar_q, t & 1, &s_abort, p.ctrl, p.dev_status);
+        ok = wait_or_abort(&bar_q, t & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status);
         tc_fence_after();
         // step 0: S_w = Q_w K_0^T (the previous tile's last PV, issued earlier,
         // has read the P held in these columns)
-        if (ok) ok = wait2(&bar_full[ks], kph, &s_abort, p.ctrl, p.dev_status);
+        if (ok) ok = wait_or_abort(&bar_full[ks], kph, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status);
         if (ok) {
 #pragma unroll
           for (int w = 0; w < NWG; ++w) issue_qk(w, ks);
@@ -376,14 +357,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ks -= NS;
             kph ^= 1;
           }
-          ok = wait2(&bar_full[vs], vph, &s_abort, p.ctrl, p.dev_status);
+          ok = wait_or_abort(&bar_full[vs], vph, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status);
         }
         // step j >= 1, per query tile w: O_w (+)= P_w V_{j-1}, then S_w = Q_w K_j^T.
         // The first PV of a tile overwrites O_w: its P hand-off comes after the
         // softmax threads have read the previous tile's O_w out of TMEM.
         for (int j = 1; j <= ti.n_kv && ok; ++j) {
           const bool qk = j < ti.n_kv;
-          if (j == ti.n_kv && !wait2(&bar_vfix[e], (t >> 1) & 1, &s_abort, p.ctrl, p.dev_status)) {
+          if (j == ti.n_kv && !wait_or_abort(&bar_vfix[e], (t >> 1) & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
             ok = false;
             break;
           }
@@ -392,7 +373,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const uint32_t kslot = ks;
 #pragma unroll
           for (int w = 0; w < NWG; ++w) {
-            if (!wait2(&bar_pfull[w], p_use[w] & 1, &s_abort, p.ctrl, p.dev_status)) {
+            if (!wait_or_abort(&bar_pfull[w], p_use[w] & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
               ok = false;
               break;
             }
@@ -413,11 +394,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               }
             }
             if (qk) {
-              if (w == 0 && !wait2(&bar_full[kslot], kph, &s_abort, p.ctrl, p.dev_status)) {
+              if (w == 0 && !wait_or_abort(&bar_full[kslot], kph, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
                 ok = false;
                 break;
               }
-              if (w == NWG - 1 && !wait2(&bar_full[vs], vph, &s_abort, p.ctrl, p.dev_status)) {
+              if (w == NWG - 1 && !wait_or_abort(&bar_full[vs], vph, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
                 ok = false;
                 break;
               }
@@ -448,7 +429,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint32_t my_s = 0;   // S hand-offs consumed by this thread
     for (uint32_t t = 0;; ++t) {
       const uint32_t e = t & 1;
-      if (!__all_sync(0xffffffffu, wait2(&bar_tfull[e], (t >> 1) & 1, &s_abort, p.ctrl, p.dev_status))) break;
+      if (!warp_wait_or_abort(&bar_tfull[e], (t >> 1) & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) break;
       const Tile2 ti = s_tile[e];
       if (!ti.valid) break;
       const int p_i = min(ti.p_first + i, ti.L - 1);
@@ -457,7 +438,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       bool ok = true;
       for (int j = 0; j < ti.n_kv && ok; ++j) {
         // S_w complete also means every earlier MMA (the PV that read P_w) is done
-        if (!__all_sync(0xffffffffu, wait2(&bar_sfull[w], my_s & 1, &s_abort, p.ctrl, p.dev_status))) {
+        if (!warp_wait_or_abort(&bar_sfull[w], my_s & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
           ok = false;
           break;
         }
@@ -533,8 +514,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_before();
         mbar_arrive(&bar_pfull[w]);
       }
-      if (ok) ok = __all_sync(0xffffffffu, wait2(&bar_odone[w], t & 1, &s_abort, p.ctrl, p.dev_status));
-      if (ok) ok = __all_sync(0xffffffffu, wait2(&bar_vfix[e], (t >> 1) & 1, &s_abort, p.ctrl, p.dev_status));
+      if (ok) ok = warp_wait_or_abort(&bar_odone[w], t & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status);
+      if (ok) ok = warp_wait_or_abort(&bar_vfix[e], (t >> 1) & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status);
       tc_fence_after();
       if (ok) {
         const int bad = s_bad[e];

@@ -18,8 +18,9 @@ namespace pkv {
 
 // Work items are 16-byte vectors: a Q/K item covers E = 16 / sizeof(T)
 // rotation pairs (E elements from each half of the row, with their E cos/sin
-// pairs); a V item is E elements copied. Consecutive threads take consecutive
-// vectors of a row, so every access is a full, coalesced 16-byte one.
+// pairs); a V item is E elements copied. A block takes a few whole tokens
+// (TokenSpan) and consecutive threads take consecutive vectors of a row, so
+// every access is a full, coalesced 16-byte one.
 template <typename T>
 __device__ __forceinline__ void rotate_vec(const T* __restrict__ src, T* __restrict__ dst, int a, int half,
                                            const float2* __restrict__ cs) {
@@ -46,7 +47,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) rope_append_kernel(const T* __restrict__ q, const T* __restrict__ k,
                                                           const T* __restrict__ v, const int32_t* __restrict__ pos,
                                                           const float2* __restrict__ cs, int32_t max_pos,
-                                                          const int64_t* __restrict__ slots, int32_t T_,
+                                                          const int64_t* __restrict__ slots, TokenSpan sp,
                                                           int32_t Hq, int32_t Hkv, int32_t D, int64_t pool_slots,
                                                           T* __restrict__ kc, T* __restrict__ vc, T* __restrict__ q_out,
                                                           int32_t* dev_status) {
@@ -55,17 +56,17 @@ __global__ void __launch_bounds__(256) rope_append_kernel(const T* __restrict__ 
   const int half = D / 2;
   const int rv = half / E;                       // rotation vectors per Q/K row
   const int cv = D / E;                          // copy vectors per V row
-  const int64_t per_token = (int64_t)(Hq + Hkv) * rv + (int64_t)Hkv * cv;
-  const int64_t total = (int64_t)T_ * per_token;
-  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t t = idx / per_token;
-    int64_t r = idx - t * per_token;
+  const int span = sp.tpb * sp.per_token;
+  for (int j = threadIdx.x; j < span; j += blockDim.x) {
+    const int tl = j / sp.per_token;
+    int r = j - tl * sp.per_token;
+    const int64_t t = (int64_t)blockIdx.x * sp.tpb + tl;
+    if (t >= sp.T) break;   // items of later tokens follow
     const int p = __ldg(pos + t);
     const int64_t slot = __ldg(slots + t);
-    if (r < (int64_t)(Hq + Hkv) * rv) {
-      const int h = (int)(r / rv);
-      const int a = (int)(r - (int64_t)h * rv) * E;
+    if (r < (Hq + Hkv) * rv) {
+      const int h = r / rv;
+      const int a = (r - h * rv) * E;
       if (p < 0 || p >= max_pos) {
         if (a == 0) atomicOr(dev_status, PKV_DEV_BAD_POSITION);
         continue;
@@ -83,10 +84,10 @@ __global__ void __launch_bounds__(256) rope_append_kernel(const T* __restrict__ 
         rotate_vec<T>(k + (t * Hkv + kh) * D, kc + (slot * Hkv + kh) * D, a, half, c);
       }
     } else {
-      r -= (int64_t)(Hq + Hkv) * rv;
+      r -= (Hq + Hkv) * rv;
       if (slot < 0 || slot >= pool_slots) continue;
-      const int vh = (int)(r / cv);
-      const int a = (int)(r - (int64_t)vh * cv) * E;
+      const int vh = r / cv;
+      const int a = (r - vh * cv) * E;
       *reinterpret_cast<uint4*>(vc + (slot * Hkv + vh) * D + a) =
           __ldg(reinterpret_cast<const uint4*>(v + (t * Hkv + vh) * D + a));
     }
@@ -96,30 +97,29 @@ __global__ void __launch_bounds__(256) rope_append_kernel(const T* __restrict__ 
 cudaError_t launch_rope_append(const void* q, const void* k, const void* v, const int32_t* positions,
                                const float* cos_sin, int32_t max_pos, const int64_t* slots, int32_t T,
                                int32_t Hq, void* kc, void* vc, void* q_out, const pkv_cache_desc& c,
-                               int32_t* dev_status, cudaStream_t s) {
+                               int32_t* dev_status, int num_sms, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int E = c.dtype == PKV_F32 ? 4 : 8;
-  const int64_t items = (int64_t)T * ((int64_t)(Hq + c.num_kv_heads) * (c.head_dim / 2 / E) +
-                                      (int64_t)c.num_kv_heads * (c.head_dim / E));
-  int64_t blocks = (items + 255) / 256;
-  if (blocks > 152 * 32) blocks = 152 * 32;
+  const int32_t per_token = (Hq + c.num_kv_heads) * (c.head_dim / 2 / E) + c.num_kv_heads * (c.head_dim / E);
+  const TokenSpan sp = token_span(T, per_token, num_sms, 2);
+  const unsigned blocks = (unsigned)sp.blocks();
   const int64_t pool_slots = (int64_t)c.num_pages * c.page_size;
   KernelTimer timer("rope_append", s);
   switch (c.dtype) {
     case PKV_F32:
-      rope_append_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(
-          (const float*)q, (const float*)k, (const float*)v, positions, (const float2*)cos_sin, max_pos, slots, T,
+      rope_append_kernel<float><<<blocks, 256, 0, s>>>(
+          (const float*)q, (const float*)k, (const float*)v, positions, (const float2*)cos_sin, max_pos, slots, sp,
           Hq, c.num_kv_heads, c.head_dim, pool_slots, (float*)kc, (float*)vc, (float*)q_out, dev_status);
       break;
     case PKV_F16:
-      rope_append_kernel<__half><<<(unsigned)blocks, 256, 0, s>>>(
+      rope_append_kernel<__half><<<blocks, 256, 0, s>>>(
           (const __half*)q, (const __half*)k, (const __half*)v, positions, (const float2*)cos_sin, max_pos, slots,
-          T, Hq, c.num_kv_heads, c.head_dim, pool_slots, (__half*)kc, (__half*)vc, (__half*)q_out, dev_status);
+          sp, Hq, c.num_kv_heads, c.head_dim, pool_slots, (__half*)kc, (__half*)vc, (__half*)q_out, dev_status);
       break;
     default:
-      rope_append_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(
+      rope_append_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
           (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, positions,
-          (const float2*)cos_sin, max_pos, slots, T, Hq, c.num_kv_heads, c.head_dim, pool_slots,
+          (const float2*)cos_sin, max_pos, slots, sp, Hq, c.num_kv_heads, c.head_dim, pool_slots,
           (__nv_bfloat16*)kc, (__nv_bfloat16*)vc, (__nv_bfloat16*)q_out, dev_status);
   }
   return cudaGetLastError();

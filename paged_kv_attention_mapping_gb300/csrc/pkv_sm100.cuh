@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include "pagedkv.h"
+
 namespace pkv {
 namespace sm100 {
 
@@ -61,6 +63,47 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
     if ((it & 255u) == 255u && globaltimer_ns() - t0 > limit_ns) return false;
     if (it > (1u << 30)) return false;
   }
+}
+
+// The pipeline wait of every kernel of the library: wait for the phase of
+// `bar` with the given parity, while watching the CTA's abort flag. It returns
+// false, without the phase, in two cases:
+//  - another thread of the CTA gave up first and raised *abort_flag (checked
+//    every 64 polls), so the caller stops its work and drains;
+//  - about limit_ns of wall time passed (or 2^28 polls): this thread raises
+//    *abort_flag for the rest of the CTA and records PKV_DEV_TIMEOUT in the
+//    call's error word and in the device status word.
+// A protocol error thus ends the kernel with a status the host reads instead of
+// hanging the GPU. The abort flag is a CTA-shared word set to 0 before the
+// CTA's first wait.
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              int32_t* err_word, int32_t* dev_status,
+                                              uint64_t limit_ns = WAIT_LIMIT_NS) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit_ns || it > (1u << 28)) {
+        *abort_flag = 1;
+        atomicOr(err_word, PKV_DEV_TIMEOUT);
+        atomicOr(dev_status, PKV_DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// wait_or_abort by every lane of a warp, with the warp's vote: true only when
+// every lane saw the phase, so the warp leaves a loop together (the warp-wide
+// tcgen05 and shuffle instructions after the wait need all 32 lanes).
+__device__ __forceinline__ bool warp_wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                   int32_t* err_word, int32_t* dev_status,
+                                                   uint64_t limit_ns = WAIT_LIMIT_NS) {
+  return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag, err_word, dev_status, limit_ns));
 }
 
 // Make generic-proxy shared-memory writes visible to the async proxy (TMA, tcgen05).

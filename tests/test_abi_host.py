@@ -169,3 +169,43 @@ def test_attention_rejects_unsupported_shapes_on_the_host(lib):
         st = lib.pkv_paged_attention(fake, fake, fake, fake, 1, 1, heads, 1, 16, fake, fake, ctypes.byref(desc),
                                      ctypes.c_float(1.0), fake, None, fake, 1 << 20, None)
         assert st == -3, (heads, kv_heads, d, st)
+        st = lib.pkv_paged_attention_no_alloc(fake, fake, fake, fake, 1, 1, heads, 1, 16, fake, fake,
+                                              ctypes.byref(desc), ctypes.c_float(1.0), fake, None, None)
+        assert st == -3, (heads, kv_heads, d, st)
+
+
+def test_no_alloc_rejects_oversized_plans_on_the_host(lib):
+    """A tick whose per-row plan does not fit the fixed scratch array is refused
+    with PKV_E_WORKSPACE before the array or the device is touched."""
+    import ctypes
+    fake = ctypes.c_void_p(256)
+    desc = binding.CacheDesc(4, 16, 2, 64, binding.PKV_BF16)
+    st = lib.pkv_paged_attention_no_alloc(fake, fake, fake, fake, 1, 2_000_000, 8, 1, 16, fake, fake,
+                                          ctypes.byref(desc), ctypes.c_float(0.1), fake, None, None)
+    assert st == -6
+    fp8 = binding.CacheDesc(4, 16, 2, 128, binding.PKV_FP8_E4M3)
+    st = lib.pkv_paged_attention_no_alloc(fake, fake, fake, fake, 1, 1, 8, 1, 16, fake, fake,
+                                          ctypes.byref(fp8), ctypes.c_float(0.1), fake, None, None)
+    assert st == -2    # fp8 caches go through pkv_paged_attention_fp8
+
+
+@pytest.mark.parametrize("call", ["paged_attention", "paged_attention_no_alloc"])
+def test_binding_rejects_host_tensors_and_wide_indices(call):
+    """The binding refuses, before any pointer reaches the library, tensors that
+    are not on the GPU and index tensors that are not int32 (a CPU pointer or a
+    64-bit table read as 32-bit ints would otherwise reach the kernels)."""
+    import torch
+    fn = getattr(binding, call)
+    kc = torch.zeros((4, 16, 2, 64), dtype=torch.bfloat16)
+    q = torch.zeros((1, 8, 64), dtype=torch.bfloat16)
+    cu = torch.tensor([0, 1], dtype=torch.int32)
+    kv = torch.tensor([1], dtype=torch.int32)
+    pt = torch.zeros((1, 1), dtype=torch.int32)
+    with pytest.raises(ValueError):
+        fn(q, cu, kv, pt, kc, kc, 0.125, 16)                     # host tensors
+    with pytest.raises(TypeError):
+        fn(q, cu.long(), kv, pt, kc, kc, 0.125, 16)              # int64 cu_seqlens_q
+    with pytest.raises(TypeError):
+        fn(q, cu, kv, pt.long(), kc, kc, 0.125, 16)              # int64 page table
+    with pytest.raises(TypeError):
+        fn(q.half(), cu, kv, pt, kc, kc, 0.125, 16)              # q dtype != cache dtype

@@ -133,6 +133,36 @@ def test_ragged(dev, case):
     run_and_compare(w, dev)
 
 
+# Page sizes that neither divide nor are multiples of the 64-key TMA tile (and
+# pages smaller than one 16-byte-aligned box) run on the CUDA-core row kernel
+# for every row, decode or chunk: it reads each key through the page table with
+# vector loads and serves all g query heads of a KV head from each load.
+ROWS_KERNEL = [
+    # seed, B, Hq, Hkv, d, P, dtype, q_lens, max_kv
+    (40, 6, 32, 8, 128, 24, "bf16", (1, 2, 17), 3000),   # rows past 2048 keys are split
+    (41, 5, 32, 4, 64, 48, "f16", (1, 17, 70), 1500),    # a 70-row chunk row by row; 512-key splits
+    (42, 4, 16, 16, 64, 24, "f32", (1, 3), 1200),        # g = 1
+    (43, 3, 16, 1, 128, 96, "f32", (1, 5), 2500),        # g = 16 at d 128
+    (44, 4, 8, 4, 128, 48, "bf16", (1, 130), 800),       # g = 2, a 130-row chunk
+    (45, 5, 8, 2, 64, 4, "f16", (1, 9), 300),            # 4-token pages
+    (46, 4, 16, 2, 64, 24, "bf16", (1,), 5000),          # g = 8, long decode rows split ten ways
+]
+
+
+@pytest.mark.parametrize("case", ROWS_KERNEL,
+                         ids=[f"s{c[0]}-{c[6]}-d{c[4]}-P{c[5]}-g{c[2] // c[3]}" for c in ROWS_KERNEL])
+def test_rows_kernel_page_sizes(dev, case):
+    seed, B, Hq, Hkv, d, P, dt, ql, mk = case
+    w = W.random_workload(seed, B, Hq, Hkv, d, P, dt, ql, mk)
+    binding.set_kernel_timing(True)
+    try:
+        run_and_compare(w, dev)
+    finally:
+        launched = binding.kernel_times()
+        binding.set_kernel_timing(False)
+    assert "rows" in launched and "decode" not in launched and "prefill_tc" not in launched, launched
+
+
 def test_chunk_among_idle_sequences_takes_row_path(dev):
     """A tick with no more rows than sequences skips the tensor-core prefill
     kernel; a 64-row chunk whose 63 companions are idle is then attended row by
@@ -378,8 +408,22 @@ def full_size_check(name, dev, n_decode=12, chunk_rows=48, seed=0):
 
     sub, rows, q_s, k_s, v_s, kc_s, vc_s = sub_problem(w, packed, seqs, host_q, host_k, host_v,
                                                        pages_of(kc), pages_of(vc))
+    kc_before, vc_before = kc.clone(), vc.clone()
     out, lse = gpu_tick(w, packed, vals["q"], vals["k_new"], vals["v_new"], kc, vc, dev)
     assert binding.device_status() == 0
+    # the append over the whole tick, bit for bit: every slot of the slot
+    # mapping holds its token's K and V row, every other slot is unchanged
+    bits = torch.int32 if dt == "f32" else torch.int16
+    s_ = w.shape
+    slots_t = torch.from_numpy(packed["slot_mapping"]).to(dev)
+    for cache, before, new in ((kc, kc_before, vals["k_new"]), (vc, vc_before, vals["v_new"])):
+        flat = cache.view(-1, s_.num_kv_heads, s_.head_dim).view(bits)
+        flat_before = before.view(-1, s_.num_kv_heads, s_.head_dim).view(bits)
+        assert torch.equal(flat[slots_t], new.view(bits))
+        keep = torch.ones(flat.shape[0], dtype=torch.bool, device=dev)
+        keep[slots_t] = False
+        assert torch.equal(flat[keep], flat_before[keep])
+    del kc_before, vc_before
     # rows to check: all decode rows of the sample, and a spread of chunk rows
     sub_cu = oracle.pack_tick(*lists(sub), sub.shape.page_size)["cu_seqlens_q"]
     check = []
