@@ -483,13 +483,17 @@ def main():
     ms, eager_ms = D.max_over_ranks([ms, eager_ms], device=dev)
     value = D.aggregate_tokens_per_s(T, ms, world)
 
-    # pass B: per-kernel device time (events on the launch stream around each kernel)
+    # pass B: per-kernel device time (events on the launch stream around each
+    # kernel). The NVTX range lets a profiler select exactly these launches
+    # (ncu --nvtx --nvtx-include "kernel_timing/").
     binding.set_kernel_timing(True)
     binding.kernel_times()
+    torch.cuda.nvtx.range_push("kernel_timing")
     for _ in range(args.steps):
         flush.zero_()
         step()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     ktimes = binding.kernel_times()
     binding.set_kernel_timing(False)
     launches_per_step = sum(n for n, _ in ktimes.values()) / args.steps
