@@ -258,8 +258,11 @@ int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, const int32_
  * (q . code) * k_scale[h] * scale and the output is (sum p_j code_j) *
  * v_scale[h] / sum p_j. q is rounded to fp16 for the products with the codes
  * (every e4m3 value is exact in fp16), so bf16 queries must lie within fp16's
- * range. head_dim must be 128; page_size as for the 16-bit decode path. Every
- * row (decode and chunk rows alike) runs on the TMA-staged row kernel.
+ * range. head_dim must be 128; page_size as for the 16-bit decode path. Decode
+ * rows and short chunks run on the TMA-staged row kernel; a chunk of 64 rows
+ * or more runs on the tensor-core prefill kernel (even group sizes, scale > 0,
+ * page_size a multiple or divisor of 128), which widens each K/V tile to fp16
+ * in shared memory before its MMAs; other chunks go row by row.
  * Errors as pkv_paged_attention, plus PKV_E_DTYPE for another cache or query
  * type and PKV_E_NULL for missing scales. pkv_paged_attention answers
  * PKV_E_DTYPE for an fp8 cache. The workspace size is

@@ -263,14 +263,18 @@ int pkv::attention_impl(const void* q, int q_dtype, const int32_t* cu_seqlens_q,
   }
   cudaStream_t s = (cudaStream_t)stream;
 
-  // fp8 caches have no tensor-core prefill kernel yet: their chunk rows take the row path.
-  // A tick with no more rows than sequences is decode-only but for ticks where
-  // all rows sit in one sequence and every other sequence is idle: it skips the
-  // prefill kernel, so the decode kernel gets resident while the plan runs
-  // instead of queueing behind an empty prefill grid (any chunk of such a tick
-  // takes the row path).
-  const bool tc = !fp8 && prefill_tc_supported(cache->dtype, cache->head_dim, cache->page_size) &&
-                  total_q >= TC_MIN_Q && total_q > num_seqs;
+  // Chunks of TC_MIN_Q rows or more run on a tensor-core prefill kernel when
+  // the shape has one (fp8 caches: the two-query-tile kernel with K/V widened
+  // to fp16; other shapes take the row path). A tick with no more rows than
+  // sequences is decode-only but for ticks where all rows sit in one sequence
+  // and every other sequence is idle: it skips the prefill kernel, so the
+  // decode kernel gets resident while the plan runs instead of queueing behind
+  // an empty prefill grid (any chunk of such a tick takes the row path).
+  const bool tc_shape =
+      fp8 ? prefill_tc2_fp8_supported(q_dtype, cache->head_dim, cache->page_size, num_q_heads,
+                                      cache->num_kv_heads, scale)
+          : prefill_tc_supported(cache->dtype, cache->head_dim, cache->page_size);
+  const bool tc = tc_shape && total_q >= TC_MIN_Q && total_q > num_seqs;
 
   PlanArgs pa{};
   pa.cu = cu_seqlens_q;

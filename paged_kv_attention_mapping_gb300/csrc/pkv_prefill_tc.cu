@@ -515,6 +515,10 @@ bool prefill_tc_supported(int dtype, int D, int P) {
 }
 
 cudaError_t launch_prefill_tc(const AttnArgs& a, cudaStream_t s) {
+  if (a.kv_dtype == PKV_FP8_E4M3) {
+    if (!prefill_tc2_fp8_supported(a.dtype, a.D, a.P, a.Hq, a.Hkv, a.scale)) return cudaErrorNotSupported;
+    return launch_prefill_tc2(a, s);
+  }
   if (!prefill_tc_supported(a.dtype, a.D, a.P)) return cudaErrorNotSupported;
   if (prefill_tc2_supported(a.dtype, a.D, a.P, a.Hq, a.Hkv, a.scale)) return launch_prefill_tc2(a, s);
   KernelTimer timer("prefill_tc", s);

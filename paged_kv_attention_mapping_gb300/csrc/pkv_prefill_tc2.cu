@@ -29,6 +29,13 @@
 // reloads Q once the current tile's last QK MMA is done; the MMA thread starts
 // the next tile's first QK while the softmax warps still write the previous
 // tile's output.
+// fp8 (e4m3) caches use the same kernel with fp16 MMAs: the TMA lands each
+// K/V tile as codes in the upper half of its ring slot, two more warps
+// (10 and 11) widen the codes to fp16 in the slot's MMA layout (and narrow a
+// bf16 Q tile to fp16), and only then release the slot to the MMA thread; the
+// K scale is folded into the softmax scale and the V scale into the output
+// (mini-vLLM, "Quantization": a fused low-precision kernel instead of
+// dequantising before every matmul).
 // Every mbarrier wait is bounded (PKV_DEV_TIMEOUT); TMEM accesses are
 // warp-uniform.
 #include <cuda.h>
@@ -49,6 +56,20 @@ constexpr int BM = TC_BM;
 constexpr int BN = TC_BN;
 constexpr int NWG = 2;
 constexpr int NTHREADS = (2 + 4 * NWG) * 32;
+// fp8 caches: two more warps widen the K/V codes (and narrow a bf16 Q) for
+// the MMA; 12 warps still get the 168 registers a softmax thread needs
+constexpr int NCONV = 2;
+constexpr int NTHREADS_KV8 = NTHREADS + NCONV * 32;
+
+// What the fp8 widening warps need to know about one K/V load of the ring
+// (written by the producer before it issues the load).
+struct LoadDesc {
+  int zero_from;   // rows from here are written as zeros (BN: none)
+  int vfix_e;      // >= 0: the last V tile of the work tile in entry vfix_e
+  int q_first;     // narrow this work tile's Q (bf16 queries) before the tile
+  int q_par;       // parity of that Q load
+  int stop;        // no more loads: the widening warps leave
+};
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.f;
 
@@ -63,6 +84,8 @@ struct Params2 {
   int32_t* ctrl;
   const int2* pairs;
   int32_t* dev_status;
+  const float* k_scale;  // fp8 caches: per-KV-head dequantisation scales (> 0), else null
+  const float* v_scale;
 };
 
 struct Tile2 {
@@ -108,11 +131,77 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
   }
 }
 
-template <int D, typename T>
-__global__ void __launch_bounds__(NTHREADS, 1)
+// Two e4m3 codes (the low 16 bits, first element in the low byte) -> two fp16
+// values packed (first in the low half). Exact: every e4m3 value, NaN included,
+// is an fp16 value. (Measured against an integer-and-multiply widening on the
+// mixed tick over an fp8 cache: 255 vs 370 us for the attention call.)
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t codes) {
+  uint32_t out;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"((uint16_t)codes));
+  return out;
+}
+
+// fp8 caches: widen one K or V tile of e4m3 codes into the slot's 16-bit
+// layout. The codes arrive by TMA in the upper half of the slot as BN rows of
+// 128 codes (head_dim 128), 128-byte swizzled; the fp16 tile is the layout a
+// 16-bit TMA load would have made: two 64-column halves of BN 128-byte rows,
+// 128-byte swizzled (16-byte chunk c of row r at chunk c ^ (r & 7)). A lane
+// reads all 128 codes of its row before writing it, so row r of the upper half
+// (its own codes) is overwritten only after it was read. Rows >= zero_from are
+// written as zeros (the V rows past the sequence's end: 0 * (NaN code) must not
+// reach O).
+__device__ __forceinline__ void widen_rows(unsigned char* slot, int r0, int r1, int lane, int zero_from) {
+  const unsigned char* stg = slot + BN * 128;
+  for (int r = r0 + lane; r < r1; r += 32) {
+    uint4 c[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) c[k] = *reinterpret_cast<const uint4*>(stg + r * 128 + ((k ^ (r & 7)) << 4));
+    const bool z = r >= zero_from;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t w[4] = {c[k].x, c[k].y, c[k].z, c[k].w};
+      uint32_t h[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        h[2 * q] = z ? 0u : e4m3x2_to_h2(w[q]);
+        h[2 * q + 1] = z ? 0u : e4m3x2_to_h2(w[q] >> 16);
+      }
+      unsigned char* row = slot + (k >> 2) * BN * 128 + r * 128;   // dims 16k..16k+15: half k / 4
+      const int ch = (k & 3) * 2;
+      *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(row + (((ch + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+  }
+}
+
+// fp8 caches with bf16 queries: the tcgen05 f16 MMA takes both operands in one
+// type, so the Q tiles are narrowed to fp16 in place (same layout, element by
+// element, round to nearest).
+__device__ __forceinline__ void q_bf16_to_half(unsigned char* q, uint32_t bytes, int lane) {
+  uint4* v = reinterpret_cast<uint4*>(q);
+  for (uint32_t i = lane; i < bytes / 16; i += 32) {
+    uint4 x = v[i];
+    uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      __half2 h = __floats2half2_rn(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u));
+      w[k] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    v[i] = x;
+  }
+}
+
+// TQ: query/output element type. KV8: the cache holds e4m3 codes (head_dim 128);
+// the MMAs then run in fp16 on widened K/V tiles, the K scale folded into the
+// score scale and the V scale into the output.
+template <int D, typename TQ, bool KV8>
+__global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                        const __grid_constant__ CUtensorMap mv, Params2 p) {
   using C = Cfg2<D>;
+  using T = typename std::conditional<KV8, __half, TQ>::type;   // MMA operand type
+  constexpr bool QCONV = KV8 && std::is_same<TQ, __nv_bfloat16>::value;
+  static_assert(!KV8 || D == 128, "fp8 tiles are one 128-code swizzle atom wide");
   constexpr int NS = C::NSLOT;
   constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
   extern __shared__ unsigned char smem_raw[];
@@ -125,6 +214,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // for a block-wide barrier between tiles.
   __shared__ __align__(8) uint64_t bar_q, bar_full[NS], bar_empty[NS], bar_sfull[NWG], bar_pfull[NWG],
       bar_odone[NWG], bar_qempty, bar_tfull[2], bar_tempty[2], bar_vfix[2], bar_drain;
+  // fp8 caches: the TMA lands codes (bar_tma) and Q (bar_qtma); the widening
+  // warps convert them and only then arrive on bar_full / bar_q / bar_vfix
+  __shared__ __align__(8) uint64_t bar_tma[KV8 ? NS : 1], bar_qtma;
+  __shared__ LoadDesc s_ld[KV8 ? NS : 1];
   __shared__ uint32_t s_tmem;
   __shared__ Tile2 s_tile[2];
   __shared__ volatile int s_abort;
@@ -139,9 +232,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // may start as soon as every CTA here has passed pdl_trigger
   if ((int)blockIdx.x >= *(volatile const int32_t*)&p.ctrl[CTRL_PF_CTAS]) return;
   if (tid == 0) {
-    mbar_init(&bar_q, 1);
+    mbar_init(&bar_q, QCONV ? NCONV : 1);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_full[s], KV8 ? NCONV : 1);
       mbar_init(&bar_empty[s], 1);
     }
     for (int w = 0; w < NWG; ++w) {
@@ -153,9 +246,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int e = 0; e < 2; ++e) {
       mbar_init(&bar_tfull[e], 1);
       mbar_init(&bar_tempty[e], 1 + 4 * NWG);   // the MMA thread and every softmax warp
-      mbar_init(&bar_vfix[e], 1);
+      mbar_init(&bar_vfix[e], KV8 ? NCONV : 1);
     }
     mbar_init(&bar_drain, 1);
+    if constexpr (KV8) {
+      for (int s = 0; s < NS; ++s) mbar_init(&bar_tma[s], 1);
+      mbar_init(&bar_qtma, 1);
+    }
     fence_mbar_init();
     s_abort = 0;
     tma_prefetch_desc(&mq);
@@ -223,12 +320,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         break;
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bar_q, NWG * C::Q_BYTES);
+        // fp8 caches with bf16 queries: Q lands on bar_qtma and the widening
+        // warps narrow it to fp16 before bar_q releases it to the MMA thread
+        uint64_t* qbar = QCONV ? &bar_qtma : &bar_q;
+        mbar_arrive_expect_tx(qbar, NWG * C::Q_BYTES);
 #pragma unroll
         for (int w = 0; w < NWG; ++w)
 #pragma unroll
           for (int hf = 0; hf < C::HALVES; ++hf)
-            tma_load_3d(sQ + w * C::Q_BYTES + hf * BM * 128, &mq, &bar_q, hf * 64, ti.h + w, ti.row0);
+            tma_load_3d(sQ + w * C::Q_BYTES + hf * BM * 128, &mq, qbar, hf * 64, ti.h + w, ti.row0);
       }
       const int n_pages_seq = (ti.L + p.P - 1) / p.P;
       for (int j = 0; j < ti.n_kv && ok; ++j) {
@@ -241,6 +341,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           unsigned char* dst = sRing + slot * C::SLOT_BYTES;
           const CUtensorMap* map = kv == 0 ? &mk : &mv;
+          // 16-bit caches load straight into the MMA layout; fp8 codes land in
+          // the upper half of the slot (one 128-code box per page run)
+          uint64_t* lbar = KV8 ? &bar_tma[slot] : &bar_full[slot];
+          unsigned char* ldst = KV8 ? dst + BN * 128 : dst;
+          constexpr int LD_HALVES = KV8 ? 1 : C::HALVES;
+          constexpr uint32_t ROW_BYTES = KV8 ? D : D * 2;
+          const bool last_v = kv == 1 && j == ti.n_kv - 1;
+          if (KV8 && lane == 0) {
+            // read by the widening warps once this load's barrier completes
+            LoadDesc d;
+            d.zero_from = last_v ? ti.zero_from : BN;
+            d.vfix_e = last_v ? (int)e : -1;
+            d.q_first = QCONV && j == 0 && kv == 0;
+            d.q_par = t & 1;
+            d.stop = 0;
+            s_ld[slot] = d;
+          }
           if (lane == 0) {
             if (p.P >= BN) {
               const int lp = (j * BN) / p.P;
@@ -248,12 +365,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               const int page = pt[lp];
               if (page < 0 || page >= p.num_pages) {
                 atomicOr(&s_bad[e], 1);
-                mbar_arrive(&bar_full[slot]);
+                mbar_arrive(lbar);
               } else {
-                mbar_arrive_expect_tx(&bar_full[slot], C::SLOT_BYTES);
+                mbar_arrive_expect_tx(lbar, BN * ROW_BYTES);
 #pragma unroll
-                for (int hf = 0; hf < C::HALVES; ++hf)
-                  tma_load_3d(dst + hf * BN * 128, map, &bar_full[slot], hf * 64, ti.kvh, page * p.P + off);
+                for (int hf = 0; hf < LD_HALVES; ++hf)
+                  tma_load_3d(ldst + hf * BN * 128, map, lbar, hf * 64, ti.kvh, page * p.P + off);
               }
             } else {
               const int per = BN / p.P;
@@ -266,21 +383,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               }
               if (bad) {
                 atomicOr(&s_bad[e], 1);
-                mbar_arrive(&bar_full[slot]);
+                mbar_arrive(lbar);
               } else {
-                mbar_arrive_expect_tx(&bar_full[slot], (uint32_t)cnt * p.P * D * 2);
+                mbar_arrive_expect_tx(lbar, (uint32_t)cnt * p.P * ROW_BYTES);
                 for (int pp = 0; pp < cnt; ++pp) {
                   const int page = pt[lp0 + pp];
 #pragma unroll
-                  for (int hf = 0; hf < C::HALVES; ++hf)
-                    tma_load_3d(dst + hf * BN * 128 + pp * p.P * 128, map, &bar_full[slot], hf * 64, ti.kvh,
-                                page * p.P);
+                  for (int hf = 0; hf < LD_HALVES; ++hf)
+                    tma_load_3d(ldst + hf * BN * 128 + pp * p.P * 128, map, lbar, hf * 64, ti.kvh, page * p.P);
                 }
               }
             }
           }
           fills[slot] += 1;
-          if (kv == 1 && j == ti.n_kv - 1) {
+          if constexpr (KV8) {
+            // the widening warps zero the V rows past the end and arrive on bar_vfix
+          } else if (last_v) {
             if (ti.zero_from < BN) {
               if (!warp_wait_or_abort(&bar_full[slot], round & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
                 ok = false;
@@ -298,9 +416,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
     }
+    if constexpr (KV8) {
+      // no more loads: let the widening warps leave (the slot's previous load
+      // must be consumed before its descriptor is rewritten)
+      const uint32_t slot = ring % NS, round = ring / NS;
+      if (ok && warp_wait_or_abort(&bar_empty[slot], (round & 1) ^ 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status) &&
+          lane == 0) {
+        s_ld[slot].stop = 1;
+        mbar_arrive(&bar_tma[slot]);
+      }
+    }
     if (!ok && lane == 0) {
+      // let every copy this warp issued land before the CTA may exit
       for (int s = 0; s < NS; ++s)
-        if (fills[s] > 0) mbar_wait(&bar_full[s], (fills[s] - 1) & 1, 500000000ull);
+        if (fills[s] > 0) mbar_wait(KV8 ? &bar_tma[s] : &bar_full[s], (fills[s] - 1) & 1, 500000000ull);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
@@ -419,6 +548,39 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (ok) mbar_arrive(&bar_tempty[e]);
       }
     }
+  } else if (KV8 && warp >= 2 + 4 * NWG) {
+    // -------------------------------------------------- fp8: widening warps
+    // Loads are taken in ring order; warp cw widens rows [64 cw, 64 cw + 64)
+    // of every K/V tile and narrows query tile cw of each work tile.
+    const int cw = warp - (2 + 4 * NWG);
+    constexpr int ROWS = BN / NCONV;
+    for (uint32_t n = 0;; ++n) {
+      const uint32_t slot = n % NS, par = (n / NS) & 1;
+      if (!warp_wait_or_abort(&bar_tma[slot], par, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) break;
+      // the descriptor was written before the load's barrier completed
+      const volatile LoadDesc* dv = &s_ld[slot];
+      LoadDesc d;
+      d.zero_from = dv->zero_from;
+      d.vfix_e = dv->vfix_e;
+      d.q_first = dv->q_first;
+      d.q_par = dv->q_par;
+      d.stop = dv->stop;
+      if (d.stop) break;
+      if (QCONV && d.q_first) {
+        if (!warp_wait_or_abort(&bar_qtma, d.q_par, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) break;
+        q_bf16_to_half(sQ + cw * C::Q_BYTES, C::Q_BYTES, lane);
+        fence_proxy_async_smem();   // the MMA (async proxy) reads what these threads wrote
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_q);
+      }
+      widen_rows(sRing + slot * C::SLOT_BYTES, cw * ROWS, cw * ROWS + ROWS, lane, d.zero_from);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bar_full[slot]);
+        if (d.vfix_e >= 0) mbar_arrive(&bar_vfix[d.vfix_e]);
+      }
+    }
   } else {
     // ---------------------------------------------------------------- softmax
     const int w = (warp - 2) >> 2;                // query tile of this warpgroup
@@ -433,7 +595,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const Tile2 ti = s_tile[e];
       if (!ti.valid) break;
       const int p_i = min(ti.p_first + i, ti.L - 1);
-      const float sc = p.scale_log2;
+      // fp8: the MMA multiplies q by the codes, K = codes * k_scale
+      const float sc = KV8 ? p.scale_log2 * __ldg(p.k_scale + ti.kvh) : p.scale_log2;
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
       for (int j = 0; j < ti.n_kv && ok; ++j) {
@@ -520,8 +683,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (ok) {
         const int bad = s_bad[e];
         const bool store = i < ti.nr && !bad;
-        const float inv = 1.f / l_run;
-        T* dst = (T*)p.out + ((int64_t)(ti.row0 + i) * p.Hq + ti.h + w) * D;
+        // fp8: V = codes * v_scale, applied once to the normalised output
+        const float inv = (KV8 ? __ldg(p.v_scale + ti.kvh) : 1.f) / l_run;
+        TQ* dst = (TQ*)p.out + ((int64_t)(ti.row0 + i) * p.Hq + ti.h + w) * D;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -530,10 +694,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint4 pk;
-            pk.x = pack_h2<T>(__uint_as_float(o[v * 8 + 0]) * inv, __uint_as_float(o[v * 8 + 1]) * inv);
-            pk.y = pack_h2<T>(__uint_as_float(o[v * 8 + 2]) * inv, __uint_as_float(o[v * 8 + 3]) * inv);
-            pk.z = pack_h2<T>(__uint_as_float(o[v * 8 + 4]) * inv, __uint_as_float(o[v * 8 + 5]) * inv);
-            pk.w = pack_h2<T>(__uint_as_float(o[v * 8 + 6]) * inv, __uint_as_float(o[v * 8 + 7]) * inv);
+            pk.x = pack_h2<TQ>(__uint_as_float(o[v * 8 + 0]) * inv, __uint_as_float(o[v * 8 + 1]) * inv);
+            pk.y = pack_h2<TQ>(__uint_as_float(o[v * 8 + 2]) * inv, __uint_as_float(o[v * 8 + 3]) * inv);
+            pk.z = pack_h2<TQ>(__uint_as_float(o[v * 8 + 4]) * inv, __uint_as_float(o[v * 8 + 5]) * inv);
+            pk.w = pack_h2<TQ>(__uint_as_float(o[v * 8 + 6]) * inv, __uint_as_float(o[v * 8 + 7]) * inv);
             *reinterpret_cast<uint4*>(dst + c * 32 + v * 8) = pk;
           }
         }
@@ -563,22 +727,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-template <int D, typename T>
+template <int D, typename TQ, bool KV8>
 cudaError_t launch2(const AttnArgs& a, cudaStream_t s) {
   using C = Cfg2<D>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(prefill_tc2_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    attr_err = cudaFuncSetAttribute(prefill_tc2_kernel<D, TQ, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const CUtensorMapDataType dt =
-      std::is_same<T, __nv_bfloat16>::value ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+      std::is_same<TQ, __nv_bfloat16>::value ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType kdt = KV8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : dt;
+  const int kelt = KV8 ? 1 : 2;
   CUtensorMap mq, mk, mv;
   const int box = a.P >= BN ? BN : a.P;
   if (!make_map_boxed(&mq, a.q, dt, 2, D, a.Hq, a.T, 64, BM) ||
-      !make_map_boxed(&mk, a.k_cache, dt, 2, D, a.Hkv, (int64_t)a.num_pages * a.P, 64, box) ||
-      !make_map_boxed(&mv, a.v_cache, dt, 2, D, a.Hkv, (int64_t)a.num_pages * a.P, 64, box))
+      !make_map_boxed(&mk, a.k_cache, kdt, kelt, D, a.Hkv, (int64_t)a.num_pages * a.P, 128 / kelt, box) ||
+      !make_map_boxed(&mv, a.v_cache, kdt, kelt, D, a.Hkv, (int64_t)a.num_pages * a.P, 128 / kelt, box))
     return cudaErrorInvalidValue;
   Params2 p;
   p.cu = a.cu;
@@ -597,7 +764,9 @@ cudaError_t launch2(const AttnArgs& a, cudaStream_t s) {
   p.ctrl = (int32_t*)(a.ws + a.lay.ctrl);
   p.pairs = (const int2*)(a.ws + a.lay.tc_pairs);
   p.dev_status = a.dev_status;
-  prefill_tc2_kernel<D, T><<<a.num_sms, NTHREADS, C::SMEM, s>>>(mq, mk, mv, p);
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
+  prefill_tc2_kernel<D, TQ, KV8><<<a.num_sms, KV8 ? NTHREADS_KV8 : NTHREADS, C::SMEM, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -608,10 +777,21 @@ bool prefill_tc2_supported(int dtype, int D, int P, int Hq, int Hkv, float scale
   return (Hq / Hkv) % 2 == 0 && scale > 0.f;
 }
 
+bool prefill_tc2_fp8_supported(int q_dtype, int D, int P, int Hq, int Hkv, float scale) {
+  // the page rows must split into whole 128-key tiles, as for 16-bit caches
+  if (!prefill_tc_supported(q_dtype, D, P) || D != 128) return false;
+  return (Hq / Hkv) % 2 == 0 && scale > 0.f;
+}
+
 cudaError_t launch_prefill_tc2(const AttnArgs& a, cudaStream_t s) {
   KernelTimer timer("prefill_tc", s);
-  if (a.dtype == PKV_BF16) return a.D == 64 ? launch2<64, __nv_bfloat16>(a, s) : launch2<128, __nv_bfloat16>(a, s);
-  return a.D == 64 ? launch2<64, __half>(a, s) : launch2<128, __half>(a, s);
+  if (a.kv_dtype == PKV_FP8_E4M3) {
+    if (a.D != 128) return cudaErrorNotSupported;
+    return a.dtype == PKV_BF16 ? launch2<128, __nv_bfloat16, true>(a, s) : launch2<128, __half, true>(a, s);
+  }
+  if (a.dtype == PKV_BF16)
+    return a.D == 64 ? launch2<64, __nv_bfloat16, false>(a, s) : launch2<128, __nv_bfloat16, false>(a, s);
+  return a.D == 64 ? launch2<64, __half, false>(a, s) : launch2<128, __half, false>(a, s);
 }
 
 }  // namespace pkv

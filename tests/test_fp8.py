@@ -203,9 +203,16 @@ def _fp8_tick(w, dev, qdt, seed=0, poison=True):
     ("bf16", 8, 8, 64, (1, 2, 9), 400),          # no grouping (G = 1)
     ("f16", 16, 8, 32, (1, 33), 520),            # G = 2
     ("bf16", 32, 8, 64, (1, 1, 5), 9500),        # rows split over several items, combined in the kernel
+    # chunks of 64 rows or more: the tensor-core prefill kernel with the codes
+    # widened to fp16 in shared memory (causal inside the chunk, ragged tails)
+    ("bf16", 32, 8, 256, (1, 130, 200), 1500),   # GQA 4, one page per KV tile, bf16 q narrowed to fp16
+    ("f16", 32, 8, 16, (1, 70, 129), 700),       # 16-token pages: eight pages per KV tile
+    ("bf16", 16, 8, 64, (2, 150), 600),          # G = 2, two pages per KV tile
+    ("f16", 32, 2, 128, (1, 96, 300), 900),      # G = 16
 ])
 def test_attention_over_fp8_pages(dev, qdt, Hq, Hkv, P, q_lens, max_kv):
-    w = W.random_workload(300 + Hq + P, 9, Hq, Hkv, 128, P, qdt, q_lens, max_kv)
+    seed = 300 + Hq + P + (max(q_lens) if max(q_lens) >= 64 else 0)   # chunk cases drawn apart from the rest
+    w = W.random_workload(seed, 9, Hq, Hkv, 128, P, qdt, q_lens, max_kv)
     _fp8_tick(w, dev, qdt)
 
 
@@ -249,6 +256,72 @@ def test_fp8_decode_full_size_sampled(dev):
         ro, rl = oracle.attend_row(qh[r], kseq, vseq, L, w.scale)   # a decode row sees all L keys
         assert np.abs(out[r].float().cpu().numpy() - ro).max() <= TOL_OUT["bf16"]
         assert np.abs(lse[r].cpu().numpy() - rl).max() <= TOL_LSE["bf16"]
+
+
+def _quantised_pool(w, dev, ks, vs):
+    """The workload's synthetic pool drawn on the device and quantised by the
+    library's own append (slot i <- row i), plus the tick's packing."""
+    s = w.shape
+    vals = W.device_values(w, dev)
+    N, P = w.num_pages, s.page_size
+    kc = torch.empty((N, P, s.num_kv_heads, s.head_dim), dtype=torch.uint8, device=dev)
+    vc = torch.empty_like(kc)
+    all_slots = torch.arange(N * P, dtype=torch.int64, device=dev)
+    binding.kv_append_quant(vals["k_cache"].reshape(N * P, s.num_kv_heads, s.head_dim),
+                            vals["v_cache"].reshape(N * P, s.num_kv_heads, s.head_dim), all_slots, kc, vc, ks, vs)
+    ql, kl, pg = lists(w)
+    packed = binding.pack_tick(ql, kl, pg, P, N)
+    return vals, kc, vc, packed
+
+
+@pytest.mark.gpu
+def test_fp8_mixed_tick_full_size_sampled(dev):
+    """The mixed tick (96 decode rows, two 2048-row chunks after prefixes of 0
+    and 3072, Qwen3-4B shape, page 256) over an e4m3 cache: the chunks run on
+    the tensor-core prefill kernel with widened tiles. Sampled rows of every
+    kind against the oracle over the dequantised pages."""
+    w = W.make_workload("mixed_tick")
+    s = w.shape
+    ks = torch.full((s.num_kv_heads,), 4.0 / 448.0, device=dev)
+    vs = torch.full((s.num_kv_heads,), 4.5 / 448.0, device=dev)
+    vals, kc, vc, packed = _quantised_pool(w, dev, ks, vs)
+    binding.kv_append_quant(vals["k_new"], vals["v_new"], idx_dev(packed["slot_mapping"], dev), kc, vc, ks, vs)
+    binding.set_kernel_timing(True)
+    try:
+        out, lse = binding.paged_attention_fp8(vals["q"], idx_dev(packed["cu_seqlens_q"], dev),
+                                               idx_dev(packed["kv_lens"], dev), idx_dev(packed["page_tables"], dev),
+                                               kc, vc, ks, vs, w.scale, w.max_kv_len)
+        torch.cuda.synchronize()
+    finally:
+        launched = binding.kernel_times()
+        binding.set_kernel_timing(False)
+    assert "prefill_tc" in launched, launched
+    assert binding.device_status() == 0
+    ks_h, vs_h = ks.cpu().numpy(), vs.cpu().numpy()
+    cu, kvl, pt = packed["cu_seqlens_q"], packed["kv_lens"], packed["page_tables"]
+    qh = vals["q"].float().cpu().numpy().astype(np.float64)
+    rng = np.random.default_rng(5)
+    B = len(kvl)
+    chunks = [b for b in range(B) if cu[b + 1] - cu[b] > 1]
+    rows = list(rng.choice(int(cu[len(kvl) - len(chunks)]), size=6, replace=False))
+    for b in chunks:
+        n = int(cu[b + 1] - cu[b])
+        pick = set(rng.choice(n, size=24, replace=False).tolist()) | {0, 127, 128, n - 1}
+        rows += [int(cu[b]) + j for j in sorted(pick)]
+    cache = {}
+    for r in rows:
+        b = int(np.searchsorted(cu, r, side="right") - 1)
+        L = int(kvl[b])
+        if b not in cache:
+            npg = -(-L // s.page_size)
+            pages = torch.from_numpy(pt[b, :npg].astype(np.int64)).to(dev)
+            cache[b] = (F.dequantize(kc[pages].cpu().numpy(), ks_h).reshape(-1, s.num_kv_heads, s.head_dim)[:L],
+                        F.dequantize(vc[pages].cpu().numpy(), vs_h).reshape(-1, s.num_kv_heads, s.head_dim)[:L])
+        kseq, vseq = cache[b]
+        n_visible = L - int(cu[b + 1] - cu[b]) + (r - int(cu[b])) + 1   # bottom-right causal rule
+        ro, rl = oracle.attend_row(qh[r], kseq, vseq, n_visible, w.scale)
+        assert np.abs(out[r].float().cpu().numpy() - ro).max() <= TOL_OUT["bf16"], r
+        assert np.abs(lse[r].cpu().numpy() - rl).max() <= TOL_LSE["bf16"], r
 
 
 @pytest.mark.gpu
