@@ -63,10 +63,13 @@ struct DecParams {
   void* out;
   float* lse;
   int32_t* ctrl;
-  const int32_t* item_begin;
-  const int32_t* row_seq;
-  const int32_t* row_keys;   // keys each packed row sees (row-path rows)
-  const int32_t* part_begin;
+  // the plan's row-path rows (see PlanLayout): packed row, sequence, keys,
+  // first item, first partial slot
+  const int32_t* rp_row;
+  const int32_t* rp_seq;
+  const int32_t* rp_keys;
+  const int32_t* rp_item_begin;
+  const int32_t* rp_part_begin;
   float* part_o;
   float* part_lse;
   int32_t* dev_status;
@@ -77,7 +80,7 @@ struct DecParams {
 
 struct Item {
   int valid;
-  int r, kvh, b, k0, k1, nsplit, local;   // local: partial slot of the item within its row (KV head, split)
+  int r, kvh, b, k0, k1, nsplit, part;   // part: the item's partial slot when its row is split
   int n_tiles;
 };
 
@@ -263,6 +266,7 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
   // no item in this call (every CTA reads the same word): leave before any
   // barrier set-up
   const int n_items = *(volatile const int32_t*)&p.ctrl[CTRL_N_ITEMS];
+  const int n_rp = *(volatile const int32_t*)&p.ctrl[CTRL_N_RP];
   const int Cchunk = *(volatile const int32_t*)&p.ctrl[CTRL_CHUNK];
   if (n_items == 0) {
     pdl_wait();
@@ -308,24 +312,22 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
       Item item;
       item.valid = 0;
       if (i < n_items) {
-        const int r = warp_upper_bound(p.item_begin, p.T + 1, i, lane) - 1;
-        const int b0 = __ldg(p.item_begin + r);
-        const int b1 = __ldg(p.item_begin + r + 1);
-        const int b = max(0, __ldg(p.row_seq + r));   // every row with items has its sequence here
-        const int limit = __ldg(p.row_keys + r);
-        // a row's items run split by split, the KV heads of one split next to
-        // each other, so that the heads of the same pages are read at about
-        // the same time (the heads of a key row share its DRAM pages); the
-        // partial slots stay ordered (KV head, split)
-        const int j = i - b0;
-        item.nsplit = (b1 - b0) / p.Hkv;
-        const int sp = j / p.Hkv;
-        item.kvh = j - sp * p.Hkv;
-        item.local = item.kvh * item.nsplit + sp;
-        item.r = r;
-        item.b = b;
+        // the item's row-path row, then the row's fields in one dependent
+        // round; a row's items run split by split, the KV heads of one split
+        // next to each other, so that CTAs working at the same time read the
+        // same pages (the heads of a key row share its DRAM pages)
+        const int rj = warp_upper_bound(p.rp_item_begin, n_rp + 1, i, lane) - 1;
+        const int jj = i - __ldg(p.rp_item_begin + rj);
+        const int keys = __ldg(p.rp_keys + rj);
+        const int part0 = __ldg(p.rp_part_begin + rj);
+        item.r = __ldg(p.rp_row + rj);
+        item.b = __ldg(p.rp_seq + rj);
+        const int sp = jj / p.Hkv;
+        item.kvh = jj - sp * p.Hkv;
+        item.nsplit = (keys + Cchunk - 1) / Cchunk;
         item.k0 = sp * Cchunk;
-        item.k1 = min(limit, item.k0 + Cchunk);
+        item.k1 = min(keys, item.k0 + Cchunk);
+        item.part = item.nsplit > 1 ? part0 + item.kvh * item.nsplit + sp : -1;
         item.n_tiles = (item.k1 - item.k0 + BT - 1) / BT;
         item.valid = 1;
       }
@@ -974,7 +976,7 @@ __global__ void __launch_bounds__(NTHREADS, DCfg<TKV, D, G>::CPS)
           ((T*)p.out)[((int64_t)item.r * p.Hq + item.kvh * G) * D + e] = from_f32<T>(ov);
           if (p.lse && (e - h * D) == 0) p.lse[(int64_t)item.r * p.Hq + item.kvh * G + h] = lse_n;
         } else {
-          const int pidx = __ldg(p.part_begin + item.r) + item.local;
+          const int pidx = item.part;
           p.part_o[((int64_t)pidx * G) * D + e] = ov;
           if ((e - h * D) == 0) p.part_lse[(int64_t)pidx * G + h] = lse_n;
         }
@@ -1031,10 +1033,11 @@ cudaError_t launch_dec(const AttnArgs& a, cudaStream_t s) {
   p.out = a.out;
   p.lse = a.lse;
   p.ctrl = (int32_t*)(a.ws + a.lay.ctrl);
-  p.item_begin = (const int32_t*)(a.ws + a.lay.row_item_begin);
-  p.row_seq = (const int32_t*)(a.ws + a.lay.row_seq);
-  p.row_keys = (const int32_t*)(a.ws + a.lay.row_keys);
-  p.part_begin = (const int32_t*)(a.ws + a.lay.row_part_begin);
+  p.rp_row = (const int32_t*)(a.ws + a.lay.rp_row);
+  p.rp_seq = (const int32_t*)(a.ws + a.lay.rp_seq);
+  p.rp_keys = (const int32_t*)(a.ws + a.lay.rp_keys);
+  p.rp_item_begin = (const int32_t*)(a.ws + a.lay.rp_item_begin);
+  p.rp_part_begin = (const int32_t*)(a.ws + a.lay.rp_part_begin);
   p.part_o = (float*)(a.ws + a.lay.part_o);
   p.part_lse = (float*)(a.ws + a.lay.part_lse);
   p.dev_status = a.dev_status;

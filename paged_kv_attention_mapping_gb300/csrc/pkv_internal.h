@@ -44,12 +44,23 @@ enum Ctrl : int {
   CTRL_N_PARTIALS = 7,   // partial results written
   CTRL_N_PAIRS = 8,      // (seq, q tile) pairs of the prefill kernel
   CTRL_PF_CTAS = 9,      // prefill-kernel CTAs that take tiles; the SMs of the others run decode CTAs
+  CTRL_N_RP = 10,        // row-path rows
   CTRL_WORDS = 64
 };
 
+// Row-path work. The rows that run on the decode / rows kernels ("row-path
+// rows": every row of a sequence that is not on the tensor-core prefill
+// kernel, in packed order) are numbered j = 0 .. n_rp - 1. Row j is packed
+// row rp_row[j] of sequence rp_seq[j] and sees rp_keys[j] keys, split every C
+// keys (CTRL_CHUNK) into nsplit = ceil(keys / C) splits; a split times a KV
+// head is one work item. Row j's items are rp_item_begin[j] ..
+// rp_item_begin[j + 1] - 1, split by split with the KV heads of a split
+// adjacent (item = rp_item_begin[j] + split * Hkv + kvh). A split row (more
+// than one split) writes its partial results to slots rp_part_begin[j] +
+// kvh * nsplit + split; split_rows lists those rows (j).
 struct PlanLayout {
-  size_t ctrl, row_seq, row_keys, row_item_begin, row_part_begin, split_rows, seq_pair_begin, seq_offs, tc_pairs,
-      part_lse, part_o, total;
+  size_t ctrl, rp_row, rp_seq, rp_keys, rp_item_begin, rp_part_begin, split_rows, seq_pair_begin, seq_offs,
+      tc_pairs, part_lse, part_o, total;
   int32_t partial_cap;  // partial results the workspace can hold
   int32_t pair_cap;     // (seq, q tile) pairs the workspace can hold
 };

@@ -20,17 +20,22 @@ namespace pkv {
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Per-sequence offsets of the plan (exclusive prefix sums over sequences):
+// row-path rows, work items, partial slots, split rows.
+constexpr int SEQ_OFFS = 4;
+
 PlanLayout plan_layout(int32_t B, int32_t T, int32_t Hq, int32_t Hkv, int32_t D, int32_t /*max_kv_len*/) {
   PlanLayout L{};
   size_t off = 0;
   L.ctrl = off;            off += align256(CTRL_WORDS * 4);
-  L.row_seq = off;         off += align256((size_t)T * 4 + 4);
-  L.row_keys = off;        off += align256((size_t)T * 4 + 4);
-  L.row_item_begin = off;  off += align256(((size_t)T + 1) * 4);
-  L.row_part_begin = off;  off += align256((size_t)T * 4 + 4);
+  L.rp_row = off;          off += align256((size_t)T * 4 + 4);
+  L.rp_seq = off;          off += align256((size_t)T * 4 + 4);
+  L.rp_keys = off;         off += align256((size_t)T * 4 + 4);
+  L.rp_item_begin = off;   off += align256(((size_t)T + 1) * 4);
+  L.rp_part_begin = off;   off += align256((size_t)T * 4 + 4);
   L.split_rows = off;      off += align256((size_t)T * 4 + 4);
   L.seq_pair_begin = off;  off += align256(((size_t)B + 1) * 4);
-  L.seq_offs = off;        off += align256((size_t)3 * B * 4 + 4);
+  L.seq_offs = off;        off += align256((size_t)SEQ_OFFS * B * 4 + 4);
   L.pair_cap = T / TC_BM + B + 1;
   L.tc_pairs = off;        off += align256((size_t)L.pair_cap * 8);
   const int g = Hq / Hkv;
@@ -93,26 +98,29 @@ __device__ int block_scan_excl(int v, int* total, int* sm) {
   return res;
 }
 
-// Exclusive scan of three values at once over the 1024 threads of the block.
-__device__ void block_scan3(const int (&v)[3], int (&ex)[3], int (&tot)[3], int (*sm)[32]) {
+// Exclusive scan of N values at once over the 1024 threads of the block.
+template <int N>
+__device__ void block_scan_n(const int (&v)[N], int (&ex)[N], int (&tot)[N], int (*sm)[32]) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  int x[3] = {v[0], v[1], v[2]};
+  int x[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) x[k] = v[k];
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
+    for (int k = 0; k < N; ++k) {
       const int y = __shfl_up_sync(0xffffffffu, x[k], o);
       if (lane >= o) x[k] += y;
     }
   }
   if (lane == 31) {
 #pragma unroll
-    for (int k = 0; k < 3; ++k) sm[k][w] = x[k];
+    for (int k = 0; k < N; ++k) sm[k][w] = x[k];
   }
   __syncthreads();
   if (w == 0) {
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
+    for (int k = 0; k < N; ++k) {
       int s = sm[k][lane];
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -124,7 +132,7 @@ __device__ void block_scan3(const int (&v)[3], int (&ex)[3], int (&tot)[3], int 
   }
   __syncthreads();
 #pragma unroll
-  for (int k = 0; k < 3; ++k) {
+  for (int k = 0; k < N; ++k) {
     ex[k] = (w > 0 ? sm[k][w - 1] : 0) + x[k] - v[k];
     tot[k] = sm[k][31];
   }
@@ -132,6 +140,7 @@ __device__ void block_scan3(const int (&v)[3], int (&ex)[3], int (&tot)[3], int 
 }
 
 constexpr int HIST = 2048;
+constexpr int RANK_SORT_MAX = 256;   // up to this many prefill pairs are ranked directly
 
 struct SeqInfo {
   int c0, q, L;
@@ -186,7 +195,10 @@ __device__ int prefill_ctas(const PlanArgs& a, int n_pairs, unsigned long long s
   return x < lo ? lo : (x > N ? N : x);
 }
 
-constexpr int PLAN_SMEM_SEQS = 8192;   // sequences whose lengths and offsets are staged in shared memory
+// sequences whose lengths and offsets are staged in shared memory:
+// cu (B + 1), kv_lens (B), pair offsets (B + 1) and SEQ_OFFS offsets per sequence
+constexpr int PLAN_SMEM_SEQS = 6144;
+constexpr int PLAN_SMEM_WORDS = (3 + SEQ_OFFS) * PLAN_SMEM_SEQS + 2;
 
 __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_status) {
   // stage cu_seqlens_q and kv_lens in shared memory: every row below searches them
@@ -202,14 +214,16 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
     __syncthreads();
   }
   int32_t* ctrl = (int32_t*)(a.ws + a.lay.ctrl);
-  int32_t* row_seq = (int32_t*)(a.ws + a.lay.row_seq);
-  int32_t* row_keys = (int32_t*)(a.ws + a.lay.row_keys);
-  int32_t* item_begin = (int32_t*)(a.ws + a.lay.row_item_begin);
-  int32_t* part_begin = (int32_t*)(a.ws + a.lay.row_part_begin);
+  int32_t* rp_row = (int32_t*)(a.ws + a.lay.rp_row);
+  int32_t* rp_seq = (int32_t*)(a.ws + a.lay.rp_seq);
+  int32_t* rp_keys = (int32_t*)(a.ws + a.lay.rp_keys);
+  int32_t* rp_item_begin = (int32_t*)(a.ws + a.lay.rp_item_begin);
+  int32_t* rp_part_begin = (int32_t*)(a.ws + a.lay.rp_part_begin);
   int32_t* split_rows = (int32_t*)(a.ws + a.lay.split_rows);
   int32_t* pair_begin_g = (int32_t*)(a.ws + a.lay.seq_pair_begin);
   int32_t* pair_begin = staged ? s_seq + 2 * a_in.B + 1 : pair_begin_g;
-  // per sequence: first item, first partial slot, first split-row index
+  // per sequence: the SEQ_OFFS offsets (row-path rows, items, partial slots,
+  // split rows)
   volatile int32_t* seq_off = staged ? s_seq + 3 * a_in.B + 2 : (int32_t*)(a.ws + a.lay.seq_offs);
   int2* pairs = (int2*)(a.ws + a.lay.tc_pairs);
 
@@ -217,7 +231,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
   __shared__ unsigned long long s_wkeys[32], s_wsteps[32];
   __shared__ int s_err;
   __shared__ int sm[32];
-  __shared__ int sm3[3][32];
+  __shared__ int smn[SEQ_OFFS][32];
   __shared__ int hist[HIST];
   const int tid = threadIdx.x;
   const int B = a.B, Hkv = a.Hkv;
@@ -264,17 +278,18 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
   if (C > c_max) C = c_max;
   if (C < 64) C = 64;
 
-  // pass 2a: per sequence, in closed form, the items (row, KV head, split),
-  // partial slots and split rows of its rows, turned into offsets by a block
-  // scan. Row i of a row-path sequence sees k = L - q + 1 + i keys and makes
-  // ceil(k / C) items per KV head; it is split when k > C.
-  int carry[3];
+  // pass 2a: per sequence, in closed form, its row-path rows, items and
+  // partial slots, turned into offsets by a block scan. Row i of a row-path
+  // sequence sees k = L - q + 1 + i keys and makes ceil(k / C) items per KV
+  // head; it is split, with partial slots, when k > C.
+  int carry[SEQ_OFFS];
   for (int guard = 0; guard < 40; ++guard) {
-    carry[0] = carry[1] = carry[2] = 0;
+#pragma unroll
+    for (int k = 0; k < SEQ_OFFS; ++k) carry[k] = 0;
     const unsigned Cu = (unsigned)C;
     for (int base = 0; base < B; base += blockDim.x) {
       const int b = base + tid;
-      int cnt[3] = {0, 0, 0}, ex[3], tot[3];
+      int cnt[SEQ_OFFS] = {0, 0, 0, 0}, ex[SEQ_OFFS], tot[SEQ_OFFS];
       if (b < B) {
         const SeqInfo s = seq_info(a, b, partition_bad);
         if (!s.bad && !s.tc && s.q > 0) {
@@ -286,58 +301,60 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
           }
           const unsigned k_lo = (unsigned)(s.L - s.q + 1), k_hi = (unsigned)s.L;
           const long long f_hi = ceil_div_prefix(k_hi, Cu);
-          cnt[0] = (int)(f_hi - ceil_div_prefix(k_lo - 1, Cu)) * Hkv;
+          cnt[0] = s.q;
+          cnt[1] = (int)(f_hi - ceil_div_prefix(k_lo - 1, Cu)) * Hkv;
           const unsigned k_s = k_lo > Cu + 1 ? k_lo : Cu + 1;   // first split row's key count
           if (k_hi >= k_s) {
-            cnt[1] = (int)(f_hi - ceil_div_prefix(k_s - 1, Cu)) * Hkv;
-            cnt[2] = (int)(k_hi - k_s + 1);
+            cnt[2] = (int)(f_hi - ceil_div_prefix(k_s - 1, Cu)) * Hkv;
+            cnt[3] = (int)(k_hi - k_s + 1);
           }
         }
       }
-      block_scan3(cnt, ex, tot, sm3);
+      block_scan_n<SEQ_OFFS>(cnt, ex, tot, smn);
       if (b < B) {
-        seq_off[3 * b + 0] = carry[0] + ex[0];
-        seq_off[3 * b + 1] = carry[1] + ex[1];
-        seq_off[3 * b + 2] = carry[2] + ex[2];
+#pragma unroll
+        for (int k = 0; k < SEQ_OFFS; ++k) seq_off[SEQ_OFFS * b + k] = carry[k] + ex[k];
       }
 #pragma unroll
-      for (int k = 0; k < 3; ++k) carry[k] += tot[k];
+      for (int k = 0; k < SEQ_OFFS; ++k) carry[k] += tot[k];
     }
-    if (carry[1] <= a.lay.partial_cap || C >= c_max) break;
+    if (carry[2] <= a.lay.partial_cap || C >= c_max) break;
     C = C * 2 < c_max ? C * 2 : c_max;   // grow the split until the partials fit
   }
   __syncthreads();   // seq_off complete
+  const int n_rp = carry[0], n_items = carry[1], carry_parts = carry[2], carry_split = carry[3];
 
-  // pass 2b: per row (consecutive rows on consecutive threads), its sequence
-  // by binary search and its item / partial offsets from the same closed form
+  // pass 2b: per row-path row j (consecutive rows on consecutive threads), its
+  // sequence by binary search over the sequences' first row-path rows (zero-row
+  // sequences share their successor's offset, so the last sequence whose offset
+  // is <= j owns j), then its arrays from the same closed forms
   {
     const unsigned Cu = (unsigned)C;
-    for (int r = tid; r < a.T; r += blockDim.x) {
-      int bb = -1, it = 0, pt = -1, keys = 0;
-      if (!partition_bad) {
-        const int b = upper_bound_i32(a.cu, B + 1, r) - 1;   // cu[b] <= r < cu[b + 1]
-        const SeqInfo s = seq_info(a, b, false);
-        it = seq_off[3 * b];
-        if (!s.bad && !s.tc) {
-          bb = b;
-          const unsigned k_lo = (unsigned)(s.L - s.q + 1), k = k_lo + (unsigned)(r - s.c0);
-          keys = (int)k;
-          it += (int)(ceil_div_prefix(k - 1, Cu) - ceil_div_prefix(k_lo - 1, Cu)) * Hkv;
-          if (k > Cu) {
-            const unsigned k_s = k_lo > Cu + 1 ? k_lo : Cu + 1;
-            pt = seq_off[3 * b + 1] + (int)(ceil_div_prefix(k - 1, Cu) - ceil_div_prefix(k_s - 1, Cu)) * Hkv;
-            split_rows[seq_off[3 * b + 2] + (int)(k - k_s)] = r;
-          }
-        }
+    for (int j = tid; j < n_rp; j += blockDim.x) {
+      int lo = 0, hi = B;   // first b with seq_off[SEQ_OFFS * b] > j
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (seq_off[SEQ_OFFS * mid] <= j) lo = mid + 1; else hi = mid;
       }
-      row_seq[r] = bb;
-      row_keys[r] = keys;
-      item_begin[r] = it;
-      part_begin[r] = pt;
+      const int b = lo - 1;
+      const SeqInfo s = seq_info(a, b, false);
+      const int i = j - seq_off[SEQ_OFFS * b];
+      const unsigned k_lo = (unsigned)(s.L - s.q + 1), k = k_lo + (unsigned)i;
+      rp_row[j] = s.c0 + i;
+      rp_seq[j] = b;
+      rp_keys[j] = (int)k;
+      rp_item_begin[j] = seq_off[SEQ_OFFS * b + 1] +
+                         (int)(ceil_div_prefix(k - 1, Cu) - ceil_div_prefix(k_lo - 1, Cu)) * Hkv;
+      int pb = -1;
+      if (k > Cu) {
+        const unsigned k_s = k_lo > Cu + 1 ? k_lo : Cu + 1;
+        pb = seq_off[SEQ_OFFS * b + 2] + (int)(ceil_div_prefix(k - 1, Cu) - ceil_div_prefix(k_s - 1, Cu)) * Hkv;
+        split_rows[seq_off[SEQ_OFFS * b + 3] + (int)(k - k_s)] = j;
+      }
+      rp_part_begin[j] = pb;
     }
   }
-  const int carry_items = carry[0], carry_parts = carry[1], carry_split = carry[2];
-  if (tid == 0) item_begin[a.T] = carry_items;
+  if (tid == 0) rp_item_begin[n_rp] = n_items;
 
   // pass 3: (sequence, q tile) pairs of the prefill kernel, longest first
   int carry_pairs = 0;
@@ -356,19 +373,41 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
   if (tid == 0) pair_begin[a.B] = carry_pairs;
   __syncthreads();
   const int n_pairs = carry_pairs;
-  if (n_pairs > 0) {   // block-uniform
+  auto pair_work = [&](int p, int* b_out, int* qt_out) {
+    const int b = upper_bound_written(pair_begin, a.B + 1, p) - 1;   // shared memory when B fits
+    const int qt = p - pair_begin[b];
+    const SeqInfo s = seq_info(a, b, false);
+    const int q1 = min(s.q, (qt + 1) * TC_BM);
+    const int keys = s.L - s.q + q1;  // keys the tile's last row sees
+    *b_out = b;
+    *qt_out = qt;
+    return (keys + TC_BN - 1) / TC_BN;
+  };
+  if (n_pairs > 0 && n_pairs <= RANK_SORT_MAX) {   // block-uniform
+    // few pairs: thread p ranks pair p against all others (longer first, then
+    // lower index), two block barriers instead of the histogram's passes
+    int b = 0, qt = 0, w = 0;
+    if (tid < n_pairs) {
+      w = pair_work(tid, &b, &qt);
+      hist[tid] = w;
+    }
+    unsigned long long my_steps = (unsigned long long)w;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) my_steps += __shfl_xor_sync(0xffffffffu, my_steps, o);
+    if ((tid & 31) == 0) s_wsteps[tid >> 5] = my_steps;
+    __syncthreads();
+    if (tid < n_pairs) {
+      int rank = 0;
+      for (int q = 0; q < n_pairs; ++q) {
+        const int wq = hist[q];
+        rank += (wq > w || (wq == w && q < tid)) ? 1 : 0;
+      }
+      pairs[rank] = make_int2(b, qt);
+    }
+    __syncthreads();
+  } else if (n_pairs > 0) {   // block-uniform
     for (int i = tid; i < HIST; i += blockDim.x) hist[i] = 0;
     __syncthreads();
-    auto pair_work = [&](int p, int* b_out, int* qt_out) {
-      const int b = upper_bound_written(pair_begin, a.B + 1, p) - 1;   // shared memory when B fits
-      const int qt = p - pair_begin[b];
-      const SeqInfo s = seq_info(a, b, false);
-      const int q1 = min(s.q, (qt + 1) * TC_BM);
-      const int keys = s.L - s.q + q1;  // keys the tile's last row sees
-      *b_out = b;
-      *qt_out = qt;
-      return (keys + TC_BN - 1) / TC_BN;
-    };
     unsigned long long my_steps = 0;
     for (int p = tid; p < n_pairs; p += blockDim.x) {
       int b, qt;
@@ -411,7 +450,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
     for (int k = 0; k < 32; ++k) steps += s_wsteps[k];
     ctrl[CTRL_PF_CTAS] = prefill_ctas(a, n_pairs, steps, s_keys);
     ctrl[CTRL_ERR] = s_err;
-    ctrl[CTRL_N_ITEMS] = carry_items;
+    ctrl[CTRL_N_ITEMS] = n_items;
+    ctrl[CTRL_N_RP] = n_rp;
     ctrl[CTRL_ITEM_NEXT] = 0;
     ctrl[CTRL_N_PAIRS] = n_pairs;
     ctrl[CTRL_N_TILES] = n_pairs * a.Hq;
@@ -428,9 +468,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
   static cudaError_t attr = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (6 * PLAN_SMEM_SEQS + 2) * 4);
+                                                 PLAN_SMEM_WORDS * 4);
   if (attr != cudaSuccess) return attr;
-  const size_t smem = a.B <= PLAN_SMEM_SEQS ? (size_t)(6 * a.B + 2) * 4 : 0;
+  const size_t smem = a.B <= PLAN_SMEM_SEQS ? (size_t)((3 + SEQ_OFFS) * a.B + 2) * 4 : 0;
   KernelTimer timer("plan", s);
   // may overlap the preceding append, which it does not read (see pdl_wait above)
   cudaError_t e = launch_after_trigger(plan_kernel, dim3(1), dim3(1024), smem, s, a, a.dev_status);

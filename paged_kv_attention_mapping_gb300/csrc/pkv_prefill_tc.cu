@@ -114,7 +114,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __shared__ int s_bad;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  pdl_trigger();   // the decode kernel that follows reads nothing this kernel writes
+  // Launched to get resident while the plan kernel runs: wait for the plan,
+  // then let the decode kernel that follows start (it reads the plan too, and
+  // nothing this kernel writes).
+  pdl_wait();
+  pdl_trigger();
   // no tile in this call (every CTA reads the same word): leave before any
   // barrier or tensor-memory set-up
   if (*(volatile const int32_t*)&p.ctrl[CTRL_N_TILES] == 0) return;
@@ -501,7 +505,9 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t s) {
   p.ctrl = (int32_t*)(a.ws + a.lay.ctrl);
   p.pairs = (const int2*)(a.ws + a.lay.tc_pairs);
   p.dev_status = a.dev_status;
-  prefill_tc_kernel<D, T><<<a.num_sms, NTHREADS, C::SMEM, s>>>(mq, mk, mv, p);
+  const cudaError_t e =
+      launch_after_trigger(prefill_tc_kernel<D, T>, dim3(a.num_sms), dim3(NTHREADS), C::SMEM, s, mq, mk, mv, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -224,7 +224,11 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
   __shared__ int s_bad[2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  pdl_trigger();   // the decode kernel that follows reads nothing this kernel writes
+  // Launched to get resident while the plan kernel runs: wait for the plan,
+  // then let the decode kernel that follows start (it reads the plan too, and
+  // nothing this kernel writes).
+  pdl_wait();
+  pdl_trigger();
   // no tile in this call (every CTA reads the same word): leave before any
   // barrier or tensor-memory set-up
   if (*(volatile const int32_t*)&p.ctrl[CTRL_N_TILES] == 0) return;
@@ -766,7 +770,9 @@ cudaError_t launch2(const AttnArgs& a, cudaStream_t s) {
   p.dev_status = a.dev_status;
   p.k_scale = a.k_scale;
   p.v_scale = a.v_scale;
-  prefill_tc2_kernel<D, TQ, KV8><<<a.num_sms, KV8 ? NTHREADS_KV8 : NTHREADS, C::SMEM, s>>>(mq, mk, mv, p);
+  const cudaError_t e = launch_after_trigger(prefill_tc2_kernel<D, TQ, KV8>, dim3(a.num_sms),
+                                             dim3(KV8 ? NTHREADS_KV8 : NTHREADS), C::SMEM, s, mq, mk, mv, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

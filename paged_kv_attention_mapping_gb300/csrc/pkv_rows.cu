@@ -39,11 +39,15 @@ __global__ void __launch_bounds__(ROWS_WARPS * 32) rows_kernel(AttnArgs a) {
   constexpr int DPL = D / 32;  // dims per lane
   const int lane = threadIdx.x & 31;
   int32_t* ctrl = (int32_t*)(a.ws + a.lay.ctrl);
-  const int32_t* item_begin = (const int32_t*)(a.ws + a.lay.row_item_begin);
-  const int32_t* part_begin = (const int32_t*)(a.ws + a.lay.row_part_begin);
+  const int32_t* rp_row = (const int32_t*)(a.ws + a.lay.rp_row);
+  const int32_t* rp_seq = (const int32_t*)(a.ws + a.lay.rp_seq);
+  const int32_t* rp_keys = (const int32_t*)(a.ws + a.lay.rp_keys);
+  const int32_t* rp_item_begin = (const int32_t*)(a.ws + a.lay.rp_item_begin);
+  const int32_t* rp_part_begin = (const int32_t*)(a.ws + a.lay.rp_part_begin);
   float* part_o = (float*)(a.ws + a.lay.part_o);
   float* part_lse = (float*)(a.ws + a.lay.part_lse);
   const int n_items = *(volatile int32_t*)&ctrl[CTRL_N_ITEMS];
+  const int n_rp = *(volatile int32_t*)&ctrl[CTRL_N_RP];
   const int C = *(volatile int32_t*)&ctrl[CTRL_CHUNK];
   const T* __restrict__ kc = (const T*)a.k_cache;
   const T* __restrict__ vc = (const T*)a.v_cache;
@@ -56,16 +60,17 @@ __global__ void __launch_bounds__(ROWS_WARPS * 32) rows_kernel(AttnArgs a) {
     if (lane == 0) item = atomicAdd(&ctrl[CTRL_ITEM_NEXT], 1);
     item = __shfl_sync(0xffffffffu, item, 0);
     if (item >= n_items) break;
-    const int r = upper_bound_dev(item_begin, a.T + 1, item) - 1;
-    const int local = item - __ldg(item_begin + r);
-    const int nsplit = (__ldg(item_begin + r + 1) - __ldg(item_begin + r)) / a.Hkv;
-    const int kvh = local / nsplit;
-    const int sp = local - kvh * nsplit;
-    const int b = upper_bound_dev(a.cu, a.B + 1, r) - 1;
-    const int c0 = __ldg(a.cu + b);
-    const int qlen = __ldg(a.cu + b + 1) - c0;
-    const int L = __ldg(a.kv_lens + b);
-    const int limit = L - qlen + (r - c0) + 1;
+    // the item's row-path row; its items run split by split, KV heads adjacent
+    const int rj = upper_bound_dev(rp_item_begin, n_rp + 1, item) - 1;
+    const int jj = item - __ldg(rp_item_begin + rj);
+    const int limit = __ldg(rp_keys + rj);   // keys the row sees
+    const int part0 = __ldg(rp_part_begin + rj);
+    const int r = __ldg(rp_row + rj);
+    const int b = __ldg(rp_seq + rj);
+    const int sp = jj / a.Hkv;
+    const int kvh = jj - sp * a.Hkv;
+    const int nsplit = (limit + C - 1) / C;
+    const int local = kvh * nsplit + sp;      // partial slot within the row
     const int k0 = sp * C;
     const int k1 = min(limit, k0 + C);
 
@@ -156,7 +161,7 @@ __global__ void __launch_bounds__(ROWS_WARPS * 32) rows_kernel(AttnArgs a) {
         if (a.lse != nullptr && lane == 0) a.lse[(int64_t)r * a.Hq + kvh * G + h] = (m[h] + __log2f(l[h])) * LN2;
       }
     } else {
-      const int p = __ldg(part_begin + r) + local;
+      const int p = part0 + local;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float inv = 1.f / l[h];
@@ -180,9 +185,11 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnArgs a) {
   const int lane = threadIdx.x & 31;
   pdl_wait();   // launched to overlap the end of the decode kernel, whose partials it reads
   const int32_t* ctrl = (const int32_t*)(a.ws + a.lay.ctrl);
-  const int32_t* item_begin = (const int32_t*)(a.ws + a.lay.row_item_begin);
-  const int32_t* part_begin = (const int32_t*)(a.ws + a.lay.row_part_begin);
+  const int32_t* rp_row = (const int32_t*)(a.ws + a.lay.rp_row);
+  const int32_t* rp_keys = (const int32_t*)(a.ws + a.lay.rp_keys);
+  const int32_t* rp_part_begin = (const int32_t*)(a.ws + a.lay.rp_part_begin);
   const int32_t* split_rows = (const int32_t*)(a.ws + a.lay.split_rows);
+  const int C = ctrl[CTRL_CHUNK];
   const float* part_o = (const float*)(a.ws + a.lay.part_o);
   const float* part_lse = (const float*)(a.ws + a.lay.part_lse);
   const int n_rows = ctrl[CTRL_N_SPLIT_ROWS];
@@ -190,11 +197,12 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnArgs a) {
   const int64_t total = (int64_t)n_rows * a.Hq;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
   for (int64_t w = blockIdx.x * (int64_t)(blockDim.x / 32) + (threadIdx.x >> 5); w < total; w += warps) {
-    const int r = split_rows[w / a.Hq];
+    const int rj = split_rows[w / a.Hq];   // a row-path row
+    const int r = rp_row[rj];
     const int h = (int)(w % a.Hq);
     const int kvh = h / G, hh = h - kvh * G;
-    const int nsplit = (item_begin[r + 1] - item_begin[r]) / a.Hkv;
-    const int p0 = part_begin[r] + kvh * nsplit;
+    const int nsplit = (rp_keys[rj] + C - 1) / C;
+    const int p0 = rp_part_begin[rj] + kvh * nsplit;
     // lse over the splits: per-lane online max / sum, then one warp reduction
     float mx = -INFINITY, sm = 0.f;
     for (int s = lane; s < nsplit; s += 32) {
