@@ -44,6 +44,10 @@ DESCRIPTIONS = {
     "mixed_tick": ("Qwen3-4B attention shape (32/8 heads, d128, bf16, page 256): 96 decode tokens kv U[256,4096] "
                    "+ prefill chunks 2048@prefix0 and 2048@prefix3072, 4192 packed rows, appended first"),
     "shared_prefix_long": "16 decode seqs of kv 32768, 16 shared prefix pages, Qwen3-4B shape, bf16, split-KV",
+    "mixed_decode_heavy": ("Qwen3-4B attention shape, bf16, page 256: 256 decode tokens kv U[256,4096] + one "
+                           "1024-token chunk after a 2048-token prefix, 1280 packed rows, appended first"),
+    "mixed_many_chunks": ("Qwen3-4B attention shape, bf16, page 256: 32 decode tokens kv U[256,4096] + four "
+                          "512-token chunks after prefixes 0/1024/2048/4096, 2080 packed rows, appended first"),
 }
 
 

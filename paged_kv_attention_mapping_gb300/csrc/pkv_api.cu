@@ -22,6 +22,8 @@ struct DeviceFacts {
   bool ready = false;
   int ok = 0;  // 1 = sm_103
   int num_sms = 0;
+  float sm_hz = 2.07e9f;    // driver figures below; these stand in if a query fails
+  float hbm_bps = 8.18e12f;
   int32_t* status = nullptr;
 };
 static std::mutex g_dev_mu;
@@ -37,6 +39,12 @@ static const DeviceFacts* device_facts() {
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return nullptr;
     if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return nullptr;
     if (cudaDeviceGetAttribute(&f.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
+    int clk = 0, mclk = 0, bus = 0;
+    if (cudaDeviceGetAttribute(&clk, cudaDevAttrClockRate, dev) == cudaSuccess && clk > 0) f.sm_hz = clk * 1e3f;
+    if (cudaDeviceGetAttribute(&mclk, cudaDevAttrMemoryClockRate, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&bus, cudaDevAttrGlobalMemoryBusWidth, dev) == cudaSuccess && mclk > 0 && bus > 0)
+      f.hbm_bps = 2.f * (mclk * 1e3f) * (bus / 8.f);   // double data rate
+    cudaGetLastError();   // a refused query leaves no sticky error behind
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
     f.status = (int32_t*)p;
@@ -293,6 +301,11 @@ int pkv::attention_impl(const void* q, int q_dtype, const int32_t* cu_seqlens_q,
   pa.target_items = 1 << 30;
   pa.tc_min_q = tc ? TC_MIN_Q : 0;
   pa.num_sms = f->num_sms;
+  pa.sm_hz = f->sm_hz;
+  pa.hbm_bps = f->hbm_bps;
+  pa.dec_inflight_bytes = (float)decode_inflight_bytes(cache->dtype, cache->head_dim, num_q_heads / cache->num_kv_heads);
+  pa.kv8 = fp8 ? 1 : 0;
+  pa.trigger_early = tc ? 0 : 1;
   pa.D = cache->head_dim;
   pa.kv_elt = elt_bytes(cache->dtype);
   pa.share_sms = tc && decode_supported(cache->dtype, cache->head_dim, cache->page_size) && !kernel_timing_enabled();

@@ -1075,6 +1075,26 @@ cudaError_t launch_dec_d(const AttnArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+namespace {
+template <typename TKV, int D>
+int inflight_g(int group) {
+  switch (group) {
+    case 1: return DCfg<TKV, D, 1>::CPS * DCfg<TKV, D, 1>::NST * DCfg<TKV, D, 1>::STAGE_BYTES;
+    case 2: return DCfg<TKV, D, 2>::CPS * DCfg<TKV, D, 2>::NST * DCfg<TKV, D, 2>::STAGE_BYTES;
+    case 4: return DCfg<TKV, D, 4>::CPS * DCfg<TKV, D, 4>::NST * DCfg<TKV, D, 4>::STAGE_BYTES;
+    case 8: return DCfg<TKV, D, 8>::CPS * DCfg<TKV, D, 8>::NST * DCfg<TKV, D, 8>::STAGE_BYTES;
+    case 16: return DCfg<TKV, D, 16>::CPS * DCfg<TKV, D, 16>::NST * DCfg<TKV, D, 16>::STAGE_BYTES;
+    default: return 0;
+  }
+}
+}  // namespace
+
+int decode_inflight_bytes(int kv_dtype, int D, int group) {
+  if (kv_dtype == PKV_FP8_E4M3) return D == 128 ? inflight_g<uint8_t, 128>(group) : 0;
+  if (kv_dtype == PKV_F32) return D == 64 ? inflight_g<float, 64>(group) : inflight_g<float, 128>(group);
+  return D == 64 ? inflight_g<__half, 64>(group) : inflight_g<__half, 128>(group);
+}
+
 bool decode_supported(int dtype, int D, int P) {
   if (D != 64 && D != 128) return false;
   if (dtype == PKV_FP8_E4M3 && D != 128) return false;   // fp8 rows must fill a 128-byte swizzle atom

@@ -82,6 +82,10 @@ struct PlanArgs {
   int32_t target_items;           // aim for about this many row-path items
   int32_t tc_min_q;               // sequences with q_len >= this use the prefill kernel; 0 = never
   int32_t num_sms;                // SMs of the device
+  float sm_hz, hbm_bps;           // SM clock and HBM pin rate of the device (bytes / s)
+  float dec_inflight_bytes;       // bytes the decode kernel keeps in flight per SM (its stage ring)
+  int32_t kv8;                    // e4m3 cache
+  int32_t trigger_early;          // the next launch is the decode kernel: let it get resident at once
   int32_t D, kv_elt;              // head_dim and cache element bytes (decode traffic per key)
   int32_t share_sms;              // 1: the decode kernel can start beside the prefill kernel, so give
                                   //    the prefill kernel only its share of the SMs (CTRL_PF_CTAS)
@@ -187,6 +191,9 @@ cudaError_t launch_prefill_tc2(const AttnArgs& a, cudaStream_t s);
 // TMA-staged decode kernel for single rows (cudaErrorNotSupported if the shape has none).
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t s);
 bool decode_supported(int dtype, int D, int P);
+// Bytes the decode kernel keeps in flight per SM for this configuration (CTAs
+// per SM x ring stages x stage bytes); 0 when it has none.
+int decode_inflight_bytes(int kv_dtype, int D, int group);
 
 // TMA tensor map of a contiguous [rows, heads, D] tensor, 128-byte swizzled boxes.
 bool make_map_boxed(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elt, int D, int heads,

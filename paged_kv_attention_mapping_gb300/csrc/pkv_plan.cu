@@ -169,30 +169,66 @@ __device__ __forceinline__ long long ceil_div_prefix(unsigned K, unsigned C) {
 }
 
 // How many SMs the prefill kernel keeps when the decode kernel can start on
-// the others at once. Both run until their work is done, so the split aims to
-// make them end together: a prefill work tile (two 128-row query tiles of one
-// sequence and two q heads) costs an SM about as long as streaming
-// TILE_BYTES of decode K/V, and each of its KV steps (128 keys) STEP_BYTES.
-// The constants were fitted on GB300 with 128-wide heads by sweeping them on a
-// mixed tick (a KV step ~1.9 us, the start and end of a work tile less than a
-// step, against a decode kernel that streams ~85-100 GB/s per SM when it has
-// few SMs and nears the HBM limit from about half of them); 64-wide steps take
-// about three quarters as long. The split only moves time between the two
-// kernels: every tile and item is still done once.
-__device__ int prefill_ctas(const PlanArgs& a, int n_pairs, unsigned long long steps,
-                            unsigned long long row_keys) {
+// the others at once. The decode kernel streams from HBM at a rate per SM set
+// by the bytes it keeps in flight there (its TMA stage ring, a property of its
+// configuration) over the loaded memory latency, up to the HBM limit; the
+// prefill kernel's work is its KV steps and work tiles in SM cycles at the SM
+// clock. For each candidate x the model takes the time until both kernels are
+// done: the prefill on x SMs, the decode on the other N - x until the prefill
+// ends and on all N afterwards, and keeps the x with the shortest time. The
+// kernel constants were measured on GB300 (timestamp traces of the prefill
+// kernel's steps and tile boundaries; the decode kernel's rate with 16 to 48
+// SMs); the device facts (SM count and clock, HBM rate) come from the driver.
+// The split only moves time between the two kernels: every tile and item is
+// still done once.
+constexpr float PF_STEP_CYCLES_D128 = 4000.f;   // two 128-row query tiles x 128 keys, head_dim 128, 16-bit
+constexpr float PF_STEP_CYCLES_D64 = 3000.f;    // the same at head_dim 64
+constexpr float PF_STEP_CYCLES_FP8 = 4700.f;    // head_dim 128 over an e4m3 cache (tiles widened first)
+constexpr float PF_TILE_CYCLES = 1950.f;        // start and end of a work tile beyond its steps
+constexpr float DECODE_LATENCY_S = 2.3e-6f;     // loaded HBM latency of the decode kernel's TMA stream
+constexpr float HBM_STREAM_EFF = 0.83f;         // streamable fraction of the HBM pin rate (measured copy)
+
+// Evaluated by the 32 lanes of one warp (candidates strided over the lanes,
+// then a warp argmin); every lane returns the same x.
+__device__ int prefill_ctas(const PlanArgs& a, int n_pairs, unsigned long long steps, unsigned long long row_keys,
+                            int lane) {
   const int N = a.num_sms;
   if (!a.share_sms || n_pairs == 0 || row_keys == 0 || N < 3) return N;
   // fp32: this part's fp64 rate is far below its fp32 rate, and a split
   // estimate needs no more than fp32 precision
-  constexpr float TILE_BYTES = 80e3f;
-  const float step_bytes = a.D >= 128 ? 165e3f : 124e3f;
+  const float step_cycles = a.kv8 ? PF_STEP_CYCLES_FP8 : (a.D >= 128 ? PF_STEP_CYCLES_D128 : PF_STEP_CYCLES_D64);
   const float hp = (float)(a.Hq / 2);
-  const float pf = hp * ((float)steps * step_bytes + (float)n_pairs * TILE_BYTES);
-  const float dec = (float)row_keys * (float)(a.Hkv * a.D * a.kv_elt) * 2.f;
-  int x = (int)((float)N * pf / (pf + dec) + 0.5f);
-  const int lo = (N + 1) / 2;   // the decode kernel saturates HBM with about half the SMs
-  return x < lo ? lo : (x > N ? N : x);
+  const float pf = hp * ((float)steps * step_cycles + (float)n_pairs * PF_TILE_CYCLES) / a.sm_hz;   // SM-seconds
+  const float dec = (float)row_keys * (float)(a.Hkv * a.D * a.kv_elt) * 2.f;                        // bytes
+  const float bw_sm = a.dec_inflight_bytes / DECODE_LATENCY_S;
+  const float hbm = a.hbm_bps * HBM_STREAM_EFF;
+  const float r_all = fminf((float)N * bw_sm, hbm);
+  int best = N;
+  float best_t = pf / (float)N + dec / r_all;   // one after the other on every SM
+  // Below a quarter of the SMs the prefill kernel's steps run well over their
+  // cycle count beside a decode kernel that saturates HBM (its operand loads
+  // queue behind the decode stream; measured: 1024 prefill rows beside 256
+  // decode rows took 451 us with 16 prefill SMs against 376 with 32-48), so the
+  // search starts there.
+  for (int x = (N + 3) / 4 + lane; x < N; x += 32) {
+    const float t_pf = pf / (float)x;
+    const float r = fminf((float)(N - x) * bw_sm, hbm);
+    const float t = dec <= t_pf * r ? t_pf : t_pf + (dec - t_pf * r) / r_all;
+    if (t < best_t) {
+      best_t = t;
+      best = x;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ot = __shfl_xor_sync(0xffffffffu, best_t, o);
+    const int ox = __shfl_xor_sync(0xffffffffu, best, o);
+    if (ot < best_t || (ot == best_t && ox < best)) {
+      best_t = ot;
+      best = ox;
+    }
+  }
+  return best;
 }
 
 // sequences whose lengths and offsets are staged in shared memory:
@@ -203,7 +239,11 @@ constexpr int PLAN_SMEM_WORDS = (3 + SEQ_OFFS) * PLAN_SMEM_SEQS + 2;
 __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_status) {
   // stage cu_seqlens_q and kv_lens in shared memory: every row below searches them
   extern __shared__ int32_t s_seq[];
-  pdl_trigger();   // a decode kernel launched next may get resident; it waits for this grid
+  // A decode kernel launched next may get resident now (it waits for this
+  // grid). A prefill kernel launched next is let in only once the append before
+  // this kernel is done (below): its CTAs would take the registers the append
+  // still needs.
+  if (a_in.trigger_early) pdl_trigger();
   PlanArgs a = a_in;
   const bool staged = a_in.B <= PLAN_SMEM_SEQS;
   if (staged) {
@@ -445,10 +485,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
     }
     __syncthreads();
   }
-  if (tid == 0) {
+  int pf_ctas = a.num_sms;
+  if (tid < 32) {
     unsigned long long steps = 0;
     for (int k = 0; k < 32; ++k) steps += s_wsteps[k];
-    ctrl[CTRL_PF_CTAS] = prefill_ctas(a, n_pairs, steps, s_keys);
+    pf_ctas = prefill_ctas(a, n_pairs, steps, s_keys, tid);
+  }
+  if (tid == 0) {
+    ctrl[CTRL_PF_CTAS] = pf_ctas;
     ctrl[CTRL_ERR] = s_err;
     ctrl[CTRL_N_ITEMS] = n_items;
     ctrl[CTRL_N_RP] = n_rp;
@@ -464,6 +508,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
   // This kernel may have started while the preceding kernel (the append) still
   // ran; finishing only after it makes every later launch see the appended K/V.
   pdl_wait();
+  pdl_trigger();
 }
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {

@@ -88,6 +88,10 @@ WORKLOADS = (
     "qwen3_decode",        # 128 seqs, kv U[512,8192], 32/8 heads, d 128, page 256, bf16
     "mixed_tick",          # 96 decodes + 2 prefill chunks of 2048, Qwen3-4B shape, bf16
     "shared_prefix_long",  # 16 seqs of 32768, 16 shared prefix pages, Qwen3-4B shape, bf16
+    # two more packings of the mixed tick's kind, to check how the prefill /
+    # decode share of the SMs holds up away from the named tick
+    "mixed_decode_heavy",  # 256 decodes + one 1024-token chunk after 2048, Qwen3-4B shape, bf16
+    "mixed_many_chunks",   # 32 decodes + four 512-token chunks after 0/1024/2048/4096, Qwen3-4B shape
 )
 BASE_SEED = 20261202
 
@@ -138,6 +142,15 @@ def make_workload(name: str, dtype: Optional[str] = None) -> Workload:
         lens = [int(x) for x in rng.integers(256, 4096 + 1, size=96)]
         q_lens = [1] * 96 + [2048, 2048]
         kv = lens + [2048, 3072 + 2048]
+        pages, num_pages = _scatter_pages(rng, [_pages_needed(L, 256) for L in kv])
+        reqs = [Request(q, L, p) for q, L, p in zip(q_lens, kv, pages)]
+    elif name in ("mixed_decode_heavy", "mixed_many_chunks"):
+        shape = TickShape(**QWEN3_4B, dtype=dtype or "bf16")
+        n_dec, chunks = (256, [(1024, 2048)]) if name == "mixed_decode_heavy" else \
+            (32, [(512, 0), (512, 1024), (512, 2048), (512, 4096)])
+        lens = [int(x) for x in rng.integers(256, 4096 + 1, size=n_dec)]
+        q_lens = [1] * n_dec + [q for q, _ in chunks]
+        kv = lens + [pre + q for q, pre in chunks]
         pages, num_pages = _scatter_pages(rng, [_pages_needed(L, 256) for L in kv])
         reqs = [Request(q, L, p) for q, L, p in zip(q_lens, kv, pages)]
     elif name == "shared_prefix_long":

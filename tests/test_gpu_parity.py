@@ -446,6 +446,7 @@ def full_size_check(name, dev, n_decode=12, chunk_rows=48, seed=0):
     return out, lse
 
 
-@pytest.mark.parametrize("name", ["tinyllama_decode", "qwen3_decode", "mixed_tick", "shared_prefix_long"])
+@pytest.mark.parametrize("name", ["tinyllama_decode", "qwen3_decode", "mixed_tick", "shared_prefix_long",
+                                  "mixed_decode_heavy", "mixed_many_chunks"])
 def test_full_size_workload(dev, name):
     full_size_check(name, dev)
