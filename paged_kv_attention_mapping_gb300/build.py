@@ -18,7 +18,8 @@ LIB = os.path.join(HERE, "libpagedkv.so")
 BUILD = os.path.join(HERE, "_build")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 SOURCES = ["pkv_api.cu", "pkv_append.cu", "pkv_plan.cu", "pkv_rows.cu", "pkv_prefill_tc.cu", "pkv_pack.cpp",
-           "pkv_no_alloc.cu", "pkv_decode.cu", "pkv_tma.cu",
+           "pkv_no_alloc.cu", "pkv_decode.cu", "pkv_decode_bf16.cu", "pkv_decode_f16.cu", "pkv_decode_f32.cu",
+           "pkv_decode_fp8.cu", "pkv_tma.cu",
            "pkv_prefill_tc2.cu", "pkv_pool.cpp", "pkv_rope.cu", "pkv_selftest.cu"]
 
 
@@ -48,7 +49,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
         newest = max(os.path.getmtime(p) for p in deps)
         if os.path.getmtime(LIB) >= newest:
             return LIB
-    with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
         results = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
     if verbose:
         for _, log in results:

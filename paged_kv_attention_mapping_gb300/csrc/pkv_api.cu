@@ -196,7 +196,8 @@ extern "C" int pkv_rope_kv_append(const void* q, const void* k, const void* v, c
 }
 
 static bool head_dim_supported(int d) { return d == 64 || d == 128; }
-static bool group_supported(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16; }
+// q heads per KV head the kernels are built for (1 to 8, and 16)
+static bool group_supported(int g) { return (g >= 1 && g <= 8) || g == 16; }
 
 extern "C" size_t pkv_paged_attention_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
                                                      const pkv_cache_desc* cache, int32_t max_kv_len) {

@@ -252,7 +252,11 @@ static cudaError_t launch_rows_d(const AttnArgs& a, cudaStream_t s) {
   switch (a.Hq / a.Hkv) {
     case 1: return launch_rows_g<T, D, 1>(a, s);
     case 2: return launch_rows_g<T, D, 2>(a, s);
+    case 3: return launch_rows_g<T, D, 3>(a, s);
     case 4: return launch_rows_g<T, D, 4>(a, s);
+    case 5: return launch_rows_g<T, D, 5>(a, s);
+    case 6: return launch_rows_g<T, D, 6>(a, s);
+    case 7: return launch_rows_g<T, D, 7>(a, s);
     case 8: return launch_rows_g<T, D, 8>(a, s);
     case 16: return launch_rows_g<T, D, 16>(a, s);
     default: return cudaErrorNotSupported;

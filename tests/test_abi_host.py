@@ -160,11 +160,11 @@ def test_workspace_size(lib):
 
 
 def test_attention_rejects_unsupported_shapes_on_the_host(lib):
-    """Group sizes outside {1, 2, 4, 8, 16} and head_dim outside {64, 128} are
+    """Group sizes outside 1..8 and 16, and head_dim outside {64, 128}, are
     refused before any device work (PKV_E_SHAPE)."""
     import ctypes
     fake = ctypes.c_void_p(256)
-    for heads, kv_heads, d in ((24, 8, 128), (32, 8, 96), (12, 4, 128)):
+    for heads, kv_heads, d in ((40, 4, 128), (32, 8, 96), (36, 3, 128), (24, 1, 64)):
         desc = binding.CacheDesc(4, 16, kv_heads, d, binding.PKV_BF16)
         st = lib.pkv_paged_attention(fake, fake, fake, fake, 1, 1, heads, 1, 16, fake, fake, ctypes.byref(desc),
                                      ctypes.c_float(1.0), fake, None, fake, 1 << 20, None)

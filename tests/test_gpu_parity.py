@@ -123,6 +123,14 @@ RAGGED = [
     # back through its 2-entry tile ring (Q reloads, V-tail fixes, tile hand-offs)
     (18, 24, 16, 4, 128, 256, "bf16", (64, 128, 129, 200), 600),
     (19, 24, 32, 4, 64, 16, "f16", (64, 100, 150, 1), 400),
+    # groups of 3, 5, 6 and 7 q heads per KV head (the Qwen2.5 family has 5, 6
+    # and 7): decode rows on the TMA kernel, chunks on the one-tile prefill
+    # kernel (odd groups) or the two-tile kernel (6), splits
+    (51, 5, 24, 8, 128, 256, "bf16", (1, 2, 130), 2600),  # g = 3
+    (52, 5, 40, 8, 128, 128, "bf16", (1, 150), 700),      # g = 5
+    (53, 5, 12, 2, 64, 16, "f16", (1, 3, 100), 900),      # g = 6, two query tiles per CTA
+    (54, 4, 28, 4, 128, 64, "f16", (1, 130), 2300),       # g = 7
+    (55, 6, 21, 7, 64, 32, "f32", (1, 5), 1300),          # g = 3 over an fp32 cache
 ]
 
 
@@ -146,6 +154,8 @@ ROWS_KERNEL = [
     (44, 4, 8, 4, 128, 48, "bf16", (1, 130), 800),       # g = 2, a 130-row chunk
     (45, 5, 8, 2, 64, 4, "f16", (1, 9), 300),            # 4-token pages
     (46, 4, 16, 2, 64, 24, "bf16", (1,), 5000),          # g = 8, long decode rows split ten ways
+    (47, 4, 24, 4, 128, 48, "f16", (1, 70), 1200),       # g = 6
+    (48, 4, 15, 3, 64, 24, "f32", (1, 3), 900),          # g = 5
 ]
 
 
@@ -358,7 +368,7 @@ def test_decreasing_cu_seqlens_skips_every_row(dev):
 
 def test_host_checks_reject_without_launch(dev):
     kc = torch.zeros((4, 16, 2, 64), dtype=torch.bfloat16, device=dev)
-    q = torch.zeros((1, 6, 64), dtype=torch.bfloat16, device=dev)   # 6 % 4... Hq=6, Hkv=2 -> g=3 unsupported
+    q = torch.zeros((1, 24, 64), dtype=torch.bfloat16, device=dev)   # Hq=24, Hkv=2 -> g=12 unsupported
     with pytest.raises(binding.PagedKVError) as e:
         binding.paged_attention(q, torch.tensor([0, 1], dtype=torch.int32, device=dev),
                                 torch.tensor([1], dtype=torch.int32, device=dev),
