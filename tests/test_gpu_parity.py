@@ -173,6 +173,33 @@ def test_rows_kernel_page_sizes(dev, case):
     assert "rows" in launched and "decode" not in launched and "prefill_tc" not in launched, launched
 
 
+def _sweep_cases(n=24, seed=20261202):
+    """Seeded draws over the whole accepted shape space: group sizes 1-8 and 16,
+    head_dim 64/128, pages from the TMA kernels' sizes and the rows kernel's,
+    every dtype, decode rows, short chunks and chunks for the prefill kernels."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for k in range(n):
+        g = int(rng.choice([1, 2, 3, 4, 5, 6, 7, 8, 16]))
+        hkv = int(rng.choice([1, 2, 4, 8])) if g < 16 else int(rng.choice([1, 2]))
+        d = int(rng.choice([64, 128]))
+        P = int(rng.choice([8, 16, 32, 64, 128, 256, 24, 40]))
+        dt = str(rng.choice(["f32", "f16", "bf16"]))
+        ql = tuple(int(x) for x in rng.choice([1, 1, 2, 7, 64, 100, 140], size=3))
+        B = int(rng.integers(1, 7))
+        mk = int(rng.choice([200, 700, 2500]))
+        out.append((1000 + k, B, g * hkv, hkv, d, P, dt, ql, mk))
+    return out
+
+
+@pytest.mark.parametrize("case", _sweep_cases(),
+                         ids=[f"w{c[0]}-{c[6]}-d{c[4]}-P{c[5]}-g{c[2] // c[3]}" for c in _sweep_cases()])
+def test_seeded_shape_sweep(dev, case):
+    seed, B, Hq, Hkv, d, P, dt, ql, mk = case
+    w = W.random_workload(seed, B, Hq, Hkv, d, P, dt, ql, mk)
+    run_and_compare(w, dev)
+
+
 def test_chunk_among_idle_sequences_takes_row_path(dev):
     """A tick with no more rows than sequences skips the tensor-core prefill
     kernel; a 64-row chunk whose 63 companions are idle is then attended row by
