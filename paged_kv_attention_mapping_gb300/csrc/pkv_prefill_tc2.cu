@@ -105,11 +105,13 @@ struct Cfg2 {
 
 // tcgen05.mma .kind::f16 with the A operand (M x K, 16-bit, packed in pairs per
 // 32-bit column, one row per lane) in TMEM and B in shared memory.
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem]; executed by a whole warp, elect.sync picks
+// the issuing lane.
+__device__ __forceinline__ void mma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -117,6 +119,13 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// max(a, b, c) in one instruction (sm_100 family); exact, like two fmaxf.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
   return y;
 }
 
@@ -437,120 +446,130 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      // The tensor pipe holds only a few MMAs ahead of this thread, and each
-      // barrier wait or commit here costs on the order of 100 cycles, so the
-      // waits for the next operands sit behind MMAs already queued: K_j after
-      // PV_0 of step j, V_j (used in step j + 1) after PV_1. Ring slots and
-      // parities advance incrementally; descriptors are built once per operand
-      // tile and stepped by constant offsets (the start-address field is the
-      // low 14 bits, and every address stays inside shared memory).
-      const uint32_t id_qk = idesc_f16(BM, BN, BF16, false);
-      const uint32_t id_pv = idesc_f16(BM, D, BF16, true);
-      const uint32_t ring_u32 = smem_u32(sRing);
-      const uint64_t qd = smem_desc(smem_u32(sQ), 16, 1024, LAYOUT_SW128);
-      uint32_t p_use[NWG] = {0, 0};   // P hand-offs consumed per query tile
-      auto issue_qk = [&](int w, uint32_t slot) {
-        const uint64_t kd = smem_desc(ring_u32 + slot * C::SLOT_BYTES, 16, 1024, LAYOUT_SW128);
+    // The whole warp runs this loop: operands, ring positions and barrier
+    // waits are warp-uniform, and elect.sync picks the one lane that issues
+    // every MMA and commit (the same lane each time, so each commit tracks all
+    // the MMAs before it). Issued from one lane's divergent code instead, the
+    // MMA stream loses issue slots to the softmax warps of its SM
+    // sub-partition: measured on GB300, a dense FMA stream in those warps
+    // slowed back-to-back M128 N128 K16 MMAs from 64 to ~140 cycles each,
+    // against ~67 with the warp-uniform loop.
+    // The tensor pipe holds only a few MMAs ahead of the issue, and each
+    // barrier wait or commit here costs on the order of 100 cycles, so the
+    // waits for the next operands sit behind MMAs already queued: K_j after
+    // PV_0 of step j, V_j (used in step j + 1) after PV_1. Ring slots and
+    // parities advance incrementally; descriptors are built once per operand
+    // tile and stepped by constant offsets (the start-address field is the
+    // low 14 bits, and every address stays inside shared memory).
+    const uint32_t id_qk = idesc_f16(BM, BN, BF16, false);
+    const uint32_t id_pv = idesc_f16(BM, D, BF16, true);
+    const uint32_t ring_u32 = smem_u32(sRing);
+    const uint64_t qd = smem_desc(smem_u32(sQ), 16, 1024, LAYOUT_SW128);
+    uint32_t p_use[NWG] = {0, 0};   // P hand-offs consumed per query tile
+    auto issue_qk = [&](int w, uint32_t slot) {
+      const uint64_t kd = smem_desc(ring_u32 + slot * C::SLOT_BYTES, 16, 1024, LAYOUT_SW128);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * BM * 128 + (kk % 4) * 32;
-          const uint32_t offk = (kk / 4) * BN * 128 + (kk % 4) * 32;
-          mma_f16_ss(tmem + w * 128, qd + (uint64_t)((w * C::Q_BYTES + off) >> 4), kd + (uint64_t)(offk >> 4), id_qk,
-                     kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bar_sfull[w]);
-      };
-      bool ok = true;
-      for (uint32_t t = 0; ok; ++t) {
-        const uint32_t e = t & 1;
-        if (!wait_or_abort(&bar_tfull[e], (t >> 1) & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) break;
-        const Tile2 ti = s_tile[e];
-        if (!ti.valid) break;
-        // K_j is the tile's load 2j and V_j load 2j + 1 of the ring
-        uint32_t ks = ring % NS, kph = (ring / NS) & 1;
-        uint32_t vs = ks + 1, vph = kph;
-        if (vs == (uint32_t)NS) {
-          vs = 0;
-          vph ^= 1;
-        }
-        ring += 2 * ti.n_kv;
-        ok = wait_or_abort(&bar_q, t & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status);
-        tc_fence_after();
-        // step 0: S_w = Q_w K_0^T (the previous tile's last PV, issued earlier,
-        // has read the P held in these columns)
-        if (ok) ok = wait_or_abort(&bar_full[ks], kph, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status);
-        if (ok) {
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * BM * 128 + (kk % 4) * 32;
+        const uint32_t offk = (kk / 4) * BN * 128 + (kk % 4) * 32;
+        mma_f16_ss_elect(tmem + w * 128, qd + (uint64_t)((w * C::Q_BYTES + off) >> 4), kd + (uint64_t)(offk >> 4),
+                         id_qk, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_elect(&bar_sfull[w]);
+    };
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      return warp_wait_or_abort(bar, parity, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status);
+    };
+    bool ok = true;
+    for (uint32_t t = 0; ok; ++t) {
+      const uint32_t e = t & 1;
+      if (!wait(&bar_tfull[e], (t >> 1) & 1)) break;
+      const Tile2 ti = s_tile[e];
+      if (!ti.valid) break;
+      // K_j is the tile's load 2j and V_j load 2j + 1 of the ring
+      uint32_t ks = ring % NS, kph = (ring / NS) & 1;
+      uint32_t vs = ks + 1, vph = kph;
+      if (vs == (uint32_t)NS) {
+        vs = 0;
+        vph ^= 1;
+      }
+      ring += 2 * ti.n_kv;
+      ok = wait(&bar_q, t & 1);
+      tc_fence_after();
+      // step 0: S_w = Q_w K_0^T (the previous tile's last PV, issued earlier,
+      // has read the P held in these columns)
+      if (ok) ok = wait(&bar_full[ks], kph);
+      if (ok) {
 #pragma unroll
-          for (int w = 0; w < NWG; ++w) issue_qk(w, ks);
-          mma_commit(&bar_empty[ks]);
-          if (ti.n_kv == 1) mma_commit(&bar_qempty);
+        for (int w = 0; w < NWG; ++w) issue_qk(w, ks);
+        mma_commit_elect(&bar_empty[ks]);
+        if (ti.n_kv == 1) mma_commit_elect(&bar_qempty);
+        ks += 2;
+        if (ks >= (uint32_t)NS) {
+          ks -= NS;
+          kph ^= 1;
+        }
+        ok = wait(&bar_full[vs], vph);
+      }
+      // step j >= 1, per query tile w: O_w (+)= P_w V_{j-1}, then S_w = Q_w K_j^T.
+      // The first PV of a tile overwrites O_w: its P hand-off comes after the
+      // softmax threads have read the previous tile's O_w out of TMEM.
+      for (int j = 1; j <= ti.n_kv && ok; ++j) {
+        const bool qk = j < ti.n_kv;
+        if (j == ti.n_kv && !wait(&bar_vfix[e], (t >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const uint64_t vd = smem_desc(ring_u32 + vs * C::SLOT_BYTES, BN * 128, 1024, LAYOUT_SW128);
+        const uint32_t acc0 = j > 1 ? 1u : 0u;
+        const uint32_t kslot = ks;
+#pragma unroll
+        for (int w = 0; w < NWG; ++w) {
+          if (!wait(&bar_pfull[w], p_use[w] & 1)) {
+            ok = false;
+            break;
+          }
+          ++p_use[w];
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_f16_ts_elect(tmem + 256 + w * 128, tmem + w * 128 + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4),
+                             id_pv, kk > 0 ? 1u : acc0);
+          if (j == ti.n_kv) mma_commit_elect(&bar_odone[w]);
+          if (w == NWG - 1) {
+            // V_{j-1} has no reader left
+            mma_commit_elect(&bar_empty[vs]);
+            vs += 2;
+            if (vs >= (uint32_t)NS) {
+              vs -= NS;
+              vph ^= 1;
+            }
+          }
+          if (qk) {
+            if (w == 0 && !wait(&bar_full[kslot], kph)) {
+              ok = false;
+              break;
+            }
+            if (w == NWG - 1 && !wait(&bar_full[vs], vph)) {
+              ok = false;
+              break;
+            }
+            issue_qk(w, kslot);
+          }
+        }
+        if (!ok) break;
+        if (qk) {
+          mma_commit_elect(&bar_empty[kslot]);
+          if (j == ti.n_kv - 1) mma_commit_elect(&bar_qempty);
           ks += 2;
           if (ks >= (uint32_t)NS) {
             ks -= NS;
             kph ^= 1;
           }
-          ok = wait_or_abort(&bar_full[vs], vph, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status);
         }
-        // step j >= 1, per query tile w: O_w (+)= P_w V_{j-1}, then S_w = Q_w K_j^T.
-        // The first PV of a tile overwrites O_w: its P hand-off comes after the
-        // softmax threads have read the previous tile's O_w out of TMEM.
-        for (int j = 1; j <= ti.n_kv && ok; ++j) {
-          const bool qk = j < ti.n_kv;
-          if (j == ti.n_kv && !wait_or_abort(&bar_vfix[e], (t >> 1) & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
-            ok = false;
-            break;
-          }
-          const uint64_t vd = smem_desc(ring_u32 + vs * C::SLOT_BYTES, BN * 128, 1024, LAYOUT_SW128);
-          const uint32_t acc0 = j > 1 ? 1u : 0u;
-          const uint32_t kslot = ks;
-#pragma unroll
-          for (int w = 0; w < NWG; ++w) {
-            if (!wait_or_abort(&bar_pfull[w], p_use[w] & 1, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
-              ok = false;
-              break;
-            }
-            ++p_use[w];
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              mma_f16_ts(tmem + 256 + w * 128, tmem + w * 128 + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), id_pv,
-                         kk > 0 ? 1u : acc0);
-            if (j == ti.n_kv) mma_commit(&bar_odone[w]);
-            if (w == NWG - 1) {
-              // V_{j-1} has no reader left
-              mma_commit(&bar_empty[vs]);
-              vs += 2;
-              if (vs >= (uint32_t)NS) {
-                vs -= NS;
-                vph ^= 1;
-              }
-            }
-            if (qk) {
-              if (w == 0 && !wait_or_abort(&bar_full[kslot], kph, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
-                ok = false;
-                break;
-              }
-              if (w == NWG - 1 && !wait_or_abort(&bar_full[vs], vph, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status)) {
-                ok = false;
-                break;
-              }
-              issue_qk(w, kslot);
-            }
-          }
-          if (!ok) break;
-          if (qk) {
-            mma_commit(&bar_empty[kslot]);
-            if (j == ti.n_kv - 1) mma_commit(&bar_qempty);
-            ks += 2;
-            if (ks >= (uint32_t)NS) {
-              ks -= NS;
-              kph ^= 1;
-            }
-          }
-        }
-        if (ok) mbar_arrive(&bar_tempty[e]);
       }
+      if (ok && lane == 0) mbar_arrive(&bar_tempty[e]);
+      __syncwarp();
     }
   } else if (KV8 && warp >= 2 + 4 * NWG) {
     // -------------------------------------------------- fp8: widening warps
@@ -619,26 +638,27 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) reg_fence(r[c]);
-        // row max of the raw scores (scale > 0 keeps the order)
-        float mx[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+        // row max of the raw scores (scale > 0 keeps the order). The
+        // softmax threads share their SM sub-partitions with the MMA thread,
+        // whose issue slots a dense run of FMA/ALU work takes away, so the
+        // arithmetic here uses as few instructions as it can: three-input
+        // max, and fp32x2 FMA / add below.
         if (masked) {
 #pragma unroll
           for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
+            for (int e = 0; e < 32; ++e)
               if (c * 32 + e > lim) r[c][e] = __float_as_uint(-INFINITY);
-              mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(r[c][e]));
-            }
-        } else {
-#pragma unroll
-          for (int c = 0; c < BN / 32; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(r[c][e]));
         }
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sc;
+        float mx[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            mx[(e >> 1) & 7] = max3(mx[(e >> 1) & 7], __uint_as_float(r[c][e]), __uint_as_float(r[c][e + 1]));
+        const float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sc;
         const bool first = j == 0;
         const bool grow = first || mt > m_run + RESCALE_LOG2;
         const float m_new = grow ? fmaxf(mt, m_run) : m_run;
@@ -657,27 +677,28 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
         m_run = m_new;
         // P = exp2(scale * S - m) in 16-bit, packed pairs over the first 64 S
         // columns (masked keys hold -inf: exp2 gives 0 since scale > 0)
-        const float neg_m = -m_run;
-        float ls[8];
+        const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_run, -m_run);
+        float2 ls[4];   // partial row sums: ls[k] holds the keys 2k, 2k + 1 (mod 8)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+        for (int k = 0; k < 4; ++k) ls[k] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t pw[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int k0 = hf * 64 + 2 * e;
-            const float a = ex2(fmaf(__uint_as_float(r[k0 >> 5][k0 & 31]), sc, neg_m));
-            const float b = ex2(fmaf(__uint_as_float(r[(k0 + 1) >> 5][(k0 + 1) & 31]), sc, neg_m));
-            ls[(2 * e) & 7] += a;
-            ls[(2 * e + 1) & 7] += b;
+            const float2 x = __ffma2_rn(
+                make_float2(__uint_as_float(r[k0 >> 5][k0 & 31]), __uint_as_float(r[(k0 + 1) >> 5][(k0 + 1) & 31])),
+                sc2, nm2);
+            const float a = ex2(x.x), b = ex2(x.y);
+            ls[e & 3] = __fadd2_rn(ls[e & 3], make_float2(a, b));
             pw[e] = pack_h2<T>(a, b);
           }
           tmem_st32(tmem + lrow + s_col + hf * 32, pw);
           tmem_wait_st();
           reg_fence(pw);
         }
-        l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        l_run += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
         tc_fence_before();
         mbar_arrive(&bar_pfull[w]);
       }
@@ -719,10 +740,9 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
   }
 
   if (warp == 1) {
-    if (lane == 0) {
-      mma_commit(&bar_drain);
-      mbar_wait(&bar_drain, 0, 500000000ull);
-    }
+    // every MMA this warp issued is complete before TMEM is released
+    mma_commit_elect(&bar_drain);
+    mbar_wait(&bar_drain, 0, 500000000ull);
     __syncwarp();
   }
   tc_fence_before();
