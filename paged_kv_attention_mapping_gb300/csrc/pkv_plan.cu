@@ -176,15 +176,20 @@ __device__ __forceinline__ long long ceil_div_prefix(unsigned K, unsigned C) {
 // clock. For each candidate x the model takes the time until both kernels are
 // done: the prefill on x SMs, the decode on the other N - x until the prefill
 // ends and on all N afterwards, and keeps the x with the shortest time. The
-// kernel constants were measured on GB300 (timestamp traces of the prefill
-// kernel's steps and tile boundaries; the decode kernel's rate with 16 to 48
-// SMs); the device facts (SM count and clock, HBM rate) come from the driver.
-// The split only moves time between the two kernels: every tile and item is
-// still done once.
-constexpr float PF_STEP_CYCLES_D128 = 4000.f;   // two 128-row query tiles x 128 keys, head_dim 128, 16-bit
-constexpr float PF_STEP_CYCLES_D64 = 3000.f;    // the same at head_dim 64
-constexpr float PF_STEP_CYCLES_FP8 = 4700.f;    // head_dim 128 over an e4m3 cache (tiles widened first)
-constexpr float PF_TILE_CYCLES = 1950.f;        // start and end of a work tile beyond its steps
+// decode constants were measured on GB300 (the decode kernel's rate with 16 to
+// 48 SMs). The prefill constants start from the kernel's measured cycles per
+// KV step (about 3250 at head_dim 128 in long launches, ~3500 in the mixed
+// tick's chunks) and were then fitted so that the chosen x lands on the
+// measured best split (x swept in steps of 2) of five mixes: the Qwen3-shaped
+// mixed tick with 16-bit and e4m3 caches, 32 decode rows beside four 512-row
+// chunks, 192 and 256 decode rows beside two chunks (head_dim 128 and 64).
+// The device facts (SM count and clock, HBM rate) come from the driver. The
+// split only moves time between the two kernels: every tile and item is still
+// done once.
+constexpr float PF_STEP_CYCLES_D128 = 3300.f;   // two 128-row query tiles x 128 keys, head_dim 128, 16-bit
+constexpr float PF_STEP_CYCLES_D64 = 2700.f;    // the same at head_dim 64
+constexpr float PF_STEP_CYCLES_FP8 = 3900.f;    // head_dim 128 over an e4m3 cache (tiles widened first)
+constexpr float PF_TILE_CYCLES = 1700.f;        // start and end of a work tile beyond its steps
 constexpr float DECODE_LATENCY_S = 2.3e-6f;     // loaded HBM latency of the decode kernel's TMA stream
 constexpr float HBM_STREAM_EFF = 0.83f;         // streamable fraction of the HBM pin rate (measured copy)
 
@@ -205,12 +210,12 @@ __device__ int prefill_ctas(const PlanArgs& a, int n_pairs, unsigned long long s
   const float r_all = fminf((float)N * bw_sm, hbm);
   int best = N;
   float best_t = pf / (float)N + dec / r_all;   // one after the other on every SM
-  // Below a quarter of the SMs the prefill kernel's steps run well over their
-  // cycle count beside a decode kernel that saturates HBM (its operand loads
-  // queue behind the decode stream; measured: 1024 prefill rows beside 256
-  // decode rows took 451 us with 16 prefill SMs against 376 with 32-48), so the
-  // search starts there.
-  for (int x = (N + 3) / 4 + lane; x < N; x += 32) {
+  // Below about a third of the SMs the prefill kernel's steps run well over
+  // their cycle count beside a decode kernel that saturates HBM (its operand
+  // loads queue behind the decode stream; measured on ticks of 192 and 256
+  // decode rows beside two chunks: 563 and 164 us with 40 prefill SMs against
+  // 538 and 153 us with 52), so the search starts there.
+  for (int x = (N + 2) / 3 + lane; x < N; x += 32) {
     const float t_pf = pf / (float)x;
     const float r = fminf((float)(N - x) * bw_sm, hbm);
     const float t = dec <= t_pf * r ? t_pf : t_pf + (dec - t_pf * r) / r_all;

@@ -105,15 +105,23 @@ struct Cfg2 {
 
 // tcgen05.mma .kind::f16 with the A operand (M x K, 16-bit, packed in pairs per
 // 32-bit column, one row per lane) in TMEM and B in shared memory.
-// D[tmem] (+)= A[tmem] * B[smem]; executed by a whole warp, elect.sync picks
-// the issuing lane.
-__device__ __forceinline__ void mma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
-      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+// D[tmem] (+)= A[tmem] * B[smem], the warp-wide form of mma_f16_ss_warp.
+template <bool ELECT>
+__device__ __forceinline__ void mma_f16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  if constexpr (ELECT) {
+    asm volatile(
+        "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n .reg .pred p, e;\n .reg .u32 l;\n setp.ne.b32 p, %4, 0;\n mov.u32 l, %%laneid;\n"
+        " setp.eq.u32 e, l, 0;\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -453,7 +461,11 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
     // MMA stream loses issue slots to the softmax warps of its SM
     // sub-partition: measured on GB300, a dense FMA stream in those warps
     // slowed back-to-back M128 N128 K16 MMAs from 64 to ~140 cycles each,
-    // against ~67 with the warp-uniform loop.
+    // against ~67 with the warp-uniform loop. fp8 caches keep lane 0 as the
+    // issuer: there the widening warps are the bound, and the elected issue
+    // took issue slots from them (the chunks of the mixed tick over an e4m3
+    // cache: 177 us with lane 0, 183 us elected).
+    constexpr bool ELECT = !KV8;
     // The tensor pipe holds only a few MMAs ahead of the issue, and each
     // barrier wait or commit here costs on the order of 100 cycles, so the
     // waits for the next operands sit behind MMAs already queued: K_j after
@@ -472,10 +484,10 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk / 4) * BM * 128 + (kk % 4) * 32;
         const uint32_t offk = (kk / 4) * BN * 128 + (kk % 4) * 32;
-        mma_f16_ss_elect(tmem + w * 128, qd + (uint64_t)((w * C::Q_BYTES + off) >> 4), kd + (uint64_t)(offk >> 4),
+        mma_f16_ss_warp<ELECT>(tmem + w * 128, qd + (uint64_t)((w * C::Q_BYTES + off) >> 4), kd + (uint64_t)(offk >> 4),
                          id_qk, kk > 0 ? 1u : 0u);
       }
-      mma_commit_elect(&bar_sfull[w]);
+      mma_commit_warp<ELECT>(&bar_sfull[w]);
     };
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       return warp_wait_or_abort(bar, parity, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status);
@@ -502,8 +514,8 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
       if (ok) {
 #pragma unroll
         for (int w = 0; w < NWG; ++w) issue_qk(w, ks);
-        mma_commit_elect(&bar_empty[ks]);
-        if (ti.n_kv == 1) mma_commit_elect(&bar_qempty);
+        mma_commit_warp<ELECT>(&bar_empty[ks]);
+        if (ti.n_kv == 1) mma_commit_warp<ELECT>(&bar_qempty);
         ks += 2;
         if (ks >= (uint32_t)NS) {
           ks -= NS;
@@ -533,12 +545,12 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_f16_ts_elect(tmem + 256 + w * 128, tmem + w * 128 + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4),
+            mma_f16_ts_warp<ELECT>(tmem + 256 + w * 128, tmem + w * 128 + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4),
                              id_pv, kk > 0 ? 1u : acc0);
-          if (j == ti.n_kv) mma_commit_elect(&bar_odone[w]);
+          if (j == ti.n_kv) mma_commit_warp<ELECT>(&bar_odone[w]);
           if (w == NWG - 1) {
             // V_{j-1} has no reader left
-            mma_commit_elect(&bar_empty[vs]);
+            mma_commit_warp<ELECT>(&bar_empty[vs]);
             vs += 2;
             if (vs >= (uint32_t)NS) {
               vs -= NS;
@@ -559,8 +571,8 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
         }
         if (!ok) break;
         if (qk) {
-          mma_commit_elect(&bar_empty[kslot]);
-          if (j == ti.n_kv - 1) mma_commit_elect(&bar_qempty);
+          mma_commit_warp<ELECT>(&bar_empty[kslot]);
+          if (j == ti.n_kv - 1) mma_commit_warp<ELECT>(&bar_qempty);
           ks += 2;
           if (ks >= (uint32_t)NS) {
             ks -= NS;
@@ -741,7 +753,7 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
 
   if (warp == 1) {
     // every MMA this warp issued is complete before TMEM is released
-    mma_commit_elect(&bar_drain);
+    mma_commit_warp<!KV8>(&bar_drain);
     mbar_wait(&bar_drain, 0, 500000000ull);
     __syncwarp();
   }
