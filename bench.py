@@ -584,6 +584,7 @@ def main():
         avg_s = ktimes[dom][1] / ktimes[dom][0] / 1000.0
         roof = kernel_roofline(dom, ktimes, work, peaks, tag)
     roof_decode = kernel_roofline("decode", ktimes, work, peaks, tag) if "decode" in ktimes else None
+    roof_prefill = kernel_roofline("prefill_tc", ktimes, work, peaks, tag) if "prefill_tc" in ktimes else None
     app_k = "rope_append" if args.rope else ("kv_append_quant" if args.kv_fp8 else "kv_append")
     roof_append = kernel_roofline(app_k, ktimes, work, peaks, tag) if app_k in ktimes else None
     decode_k = "decode" if "decode" in ktimes else ("rows" if "rows" in ktimes else None)
@@ -607,6 +608,7 @@ def main():
         "launch": "CUDA graph replay of the step (eager launches reported under eager)",
         "roofline": roof,
         "roofline_tick": tick_roofline(work, peaks, ms),
+        "roofline_prefill": roof_prefill,
         "roofline_decode": roof_decode,
         "roofline_append": roof_append,
         "decode_hbm_gbs": decode_gbs,
