@@ -260,8 +260,8 @@ int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, const int32_
  * (every e4m3 value is exact in fp16), so bf16 queries must lie within fp16's
  * range. head_dim must be 128; page_size as for the 16-bit decode path. Decode
  * rows and short chunks run on the TMA-staged row kernel; a chunk of 64 rows
- * or more runs on the tensor-core prefill kernel (even group sizes, scale > 0,
- * page_size a multiple or divisor of 128), which widens each K/V tile to fp16
+ * or more runs on the tensor-core prefill kernel (scale > 0, page_size a
+ * multiple or divisor of 128, any group size), which widens each K/V tile to fp16
  * in shared memory before its MMAs; other chunks go row by row.
  * Errors as pkv_paged_attention, plus PKV_E_DTYPE for another cache or query
  * type and PKV_E_NULL for missing scales. pkv_paged_attention answers

@@ -181,10 +181,11 @@ cudaError_t launch_combine(const AttnArgs& a, cudaStream_t s);
 // Returns cudaErrorNotSupported when the shape has no tensor-core path.
 cudaError_t launch_prefill_tc(const AttnArgs& a, cudaStream_t s);
 bool prefill_tc_supported(int dtype, int D, int P);
-// Two query tiles (two q heads of one GQA group) per CTA; needs an even group size and scale > 0.
+// Two query tiles (two q heads of one GQA group; an odd group's last head runs
+// solo) per CTA; needs a group size of at least 2 and scale > 0.
 bool prefill_tc2_supported(int dtype, int D, int P, int Hq, int Hkv, float scale);
 // The same kernel over an fp8 e4m3 cache (K/V codes widened to fp16 in shared
-// memory; head_dim 128, even group size, q bf16 or f16).
+// memory; head_dim 128, any group size, q bf16 or f16).
 bool prefill_tc2_fp8_supported(int q_dtype, int D, int P, int Hq, int Hkv, float scale);
 // Two-query-tile kernel (16-bit caches, and fp8 caches when kv_dtype is e4m3).
 cudaError_t launch_prefill_tc2(const AttnArgs& a, cudaStream_t s);

@@ -202,7 +202,8 @@ __device__ int prefill_ctas(const PlanArgs& a, int n_pairs, unsigned long long s
   // fp32: this part's fp64 rate is far below its fp32 rate, and a split
   // estimate needs no more than fp32 precision
   const float step_cycles = a.kv8 ? PF_STEP_CYCLES_FP8 : (a.D >= 128 ? PF_STEP_CYCLES_D128 : PF_STEP_CYCLES_D64);
-  const float hp = (float)(a.Hq / 2);
+  const int g = a.Hq / a.Hkv;
+  const float hp = (float)(a.Hkv * ((g + 1) / 2));   // head pairs (an odd group's last head runs solo)
   const float pf = hp * ((float)steps * step_cycles + (float)n_pairs * PF_TILE_CYCLES) / a.sm_hz;   // SM-seconds
   const float dec = (float)row_keys * (float)(a.Hkv * a.D * a.kv_elt) * 2.f;                        // bytes
   const float bw_sm = a.dec_inflight_bytes / DECODE_LATENCY_S;

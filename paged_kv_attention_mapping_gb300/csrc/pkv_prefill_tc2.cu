@@ -88,9 +88,12 @@ struct Params2 {
   const float* v_scale;
 };
 
+// A work tile: query tile w attends q head h + w, unless solo: then the GQA
+// group has an odd size, h is its last head and query tile 1 repeats head h
+// (its MMAs and softmax run, its output is not stored).
 struct Tile2 {
   int valid;
-  int b, h, kvh, row0, nr, L, p_first, n_kv, j_mask, zero_from;
+  int b, h, kvh, solo, row0, nr, L, p_first, n_kv, j_mask, zero_from;
 };
 
 template <int D>
@@ -285,9 +288,10 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const int hpairs = p.Hq / 2;
-  const int n_tiles = *(volatile int32_t*)&p.ctrl[CTRL_N_PAIRS] * hpairs;
   const int g = p.Hq / p.Hkv;
+  const int gpairs = (g + 1) / 2;        // head pairs per GQA group (the last one solo when g is odd)
+  const int hpairs = p.Hkv * gpairs;
+  const int n_tiles = *(volatile int32_t*)&p.ctrl[CTRL_N_PAIRS] * hpairs;
 
   uint32_t ring = 0;                   // producer / MMA: K/V loads before the current tile
 
@@ -312,8 +316,11 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
         if (tt < n_tiles) {
           const int2 pr = p.pairs[tt / hpairs];
           ti.b = pr.x;
-          ti.h = (tt % hpairs) * 2;
-          ti.kvh = ti.h / g;
+          const int hp = tt % hpairs;
+          ti.kvh = hp / gpairs;
+          const int k2 = 2 * (hp - ti.kvh * gpairs);   // first head of the pair within its group
+          ti.h = ti.kvh * g + k2;
+          ti.solo = k2 + 1 < g ? 0 : 1;
           const int c0 = p.cu[ti.b];
           const int qlen = p.cu[ti.b + 1] - c0;
           ti.L = p.kv_lens[ti.b];
@@ -349,7 +356,7 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
         for (int w = 0; w < NWG; ++w)
 #pragma unroll
           for (int hf = 0; hf < C::HALVES; ++hf)
-            tma_load_3d(sQ + w * C::Q_BYTES + hf * BM * 128, &mq, qbar, hf * 64, ti.h + w, ti.row0);
+            tma_load_3d(sQ + w * C::Q_BYTES + hf * BM * 128, &mq, qbar, hf * 64, ti.h + (ti.solo ? 0 : w), ti.row0);
       }
       const int n_pages_seq = (ti.L + p.P - 1) / p.P;
       for (int j = 0; j < ti.n_kv && ok; ++j) {
@@ -719,10 +726,13 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
       tc_fence_after();
       if (ok) {
         const int bad = s_bad[e];
-        const bool store = i < ti.nr && !bad;
+        // read here, not kept live through the KV loop (registers are tight)
+        const int solo = *(volatile const int*)&s_tile[e].solo;
+        const bool store = i < ti.nr && !bad && !(solo && w == 1);
         // fp8: V = codes * v_scale, applied once to the normalised output
         const float inv = (KV8 ? __ldg(p.v_scale + ti.kvh) : 1.f) / l_run;
-        TQ* dst = (TQ*)p.out + ((int64_t)(ti.row0 + i) * p.Hq + ti.h + w) * D;
+        const int head = ti.h + (solo ? 0 : w);
+        TQ* dst = (TQ*)p.out + ((int64_t)(ti.row0 + i) * p.Hq + head) * D;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -738,7 +748,7 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
             *reinterpret_cast<uint4*>(dst + c * 32 + v * 8) = pk;
           }
         }
-        if (store && p.lse) p.lse[(int64_t)(ti.row0 + i) * p.Hq + ti.h + w] = (m_run + __log2f(l_run)) * LN2;
+        if (store && p.lse) p.lse[(int64_t)(ti.row0 + i) * p.Hq + head] = (m_run + __log2f(l_run)) * LN2;
         if (i == 0 && w == 0 && bad) {
           atomicOr(&p.ctrl[CTRL_ERR], PKV_DEV_BAD_PAGE);
           atomicOr(p.dev_status, PKV_DEV_BAD_PAGE);
@@ -810,15 +820,20 @@ cudaError_t launch2(const AttnArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+// Any group size but 1 (odd groups pair their heads and run the last one solo;
+// with one q head per KV head every tile would be solo, and the one-tile
+// kernel does that work without the second tile's idle MMAs).
 bool prefill_tc2_supported(int dtype, int D, int P, int Hq, int Hkv, float scale) {
   if (!prefill_tc_supported(dtype, D, P)) return false;
-  return (Hq / Hkv) % 2 == 0 && scale > 0.f;
+  return Hq / Hkv >= 2 && scale > 0.f;
 }
 
+// e4m3 caches have no other tensor-core prefill kernel, so every group size
+// takes this one.
 bool prefill_tc2_fp8_supported(int q_dtype, int D, int P, int Hq, int Hkv, float scale) {
   // the page rows must split into whole 128-key tiles, as for 16-bit caches
   if (!prefill_tc_supported(q_dtype, D, P) || D != 128) return false;
-  return (Hq / Hkv) % 2 == 0 && scale > 0.f;
+  return scale > 0.f;
 }
 
 cudaError_t launch_prefill_tc2(const AttnArgs& a, cudaStream_t s) {

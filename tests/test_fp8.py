@@ -209,6 +209,8 @@ def _fp8_tick(w, dev, qdt, seed=0, poison=True):
     ("f16", 32, 8, 16, (1, 70, 129), 700),       # 16-token pages: eight pages per KV tile
     ("bf16", 16, 8, 64, (2, 150), 600),          # G = 2, two pages per KV tile
     ("f16", 32, 2, 128, (1, 96, 300), 900),      # G = 16
+    ("bf16", 24, 8, 256, (1, 130, 200), 1500),   # G = 3: each group's last head runs as a solo tile
+    ("f16", 8, 8, 128, (1, 100), 600),           # G = 1: every tile solo
 ])
 def test_attention_over_fp8_pages(dev, qdt, Hq, Hkv, P, q_lens, max_kv):
     seed = 300 + Hq + P + (max(q_lens) if max(q_lens) >= 64 else 0)   # chunk cases drawn apart from the rest

@@ -124,8 +124,8 @@ RAGGED = [
     (18, 24, 16, 4, 128, 256, "bf16", (64, 128, 129, 200), 600),
     (19, 24, 32, 4, 64, 16, "f16", (64, 100, 150, 1), 400),
     # groups of 3, 5, 6 and 7 q heads per KV head (the Qwen2.5 family has 5, 6
-    # and 7): decode rows on the TMA kernel, chunks on the one-tile prefill
-    # kernel (odd groups) or the two-tile kernel (6), splits
+    # and 7): decode rows on the TMA kernel, chunks on the two-tile prefill
+    # kernel (an odd group's last head as a solo tile), splits
     (51, 5, 24, 8, 128, 256, "bf16", (1, 2, 130), 2600),  # g = 3
     (52, 5, 40, 8, 128, 128, "bf16", (1, 150), 700),      # g = 5
     (53, 5, 12, 2, 64, 16, "f16", (1, 3, 100), 900),      # g = 6, two query tiles per CTA
