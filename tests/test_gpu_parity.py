@@ -415,7 +415,7 @@ def test_host_checks_reject_without_launch(dev):
 # the named workloads at full size, on sampled sequences and rows
 
 def full_size_check(name, dev, n_decode=12, chunk_rows=48, seed=0):
-    w = W.make_workload(name)
+    w = W.make_workload(name) if isinstance(name, str) else name
     dt = w.shape.dtype
     ql, kl, pg = lists(w)
     packed = binding.pack_tick(ql, kl, pg, w.shape.page_size, w.num_pages)
@@ -487,3 +487,22 @@ def full_size_check(name, dev, n_decode=12, chunk_rows=48, seed=0):
                                   "mixed_decode_heavy", "mixed_many_chunks"])
 def test_full_size_workload(dev, name):
     full_size_check(name, dev)
+
+
+@pytest.mark.parametrize("hq,hkv", [(28, 4), (24, 8)])
+def test_full_size_mixed_tick_odd_groups(dev, hq, hkv):
+    """The mixed tick's requests (96 decodes, two 2048-row chunks) with groups of
+    7 and 3 q heads per KV head: the chunks run on the two-tile prefill kernel
+    with each group's last head as a solo tile, beside the decode rows."""
+    w0 = W.make_workload("mixed_tick")
+    s0 = w0.shape
+    shape = W.TickShape(hq, hkv, s0.head_dim, s0.page_size, s0.dtype)
+    w = W.Workload(f"mixed_tick_{hq}x{hkv}", shape, w0.requests, w0.num_pages, w0.scale, w0.seed + hq)
+    binding.set_kernel_timing(True)
+    binding.kernel_times()
+    try:
+        full_size_check(w, dev)
+        launched = binding.kernel_times()
+    finally:
+        binding.set_kernel_timing(False)
+    assert "prefill_tc" in launched and "decode" in launched, launched
