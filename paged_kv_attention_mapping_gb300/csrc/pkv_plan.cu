@@ -188,7 +188,7 @@ __device__ __forceinline__ long long ceil_div_prefix(unsigned K, unsigned C) {
 // done once.
 constexpr float PF_STEP_CYCLES_D128 = 3300.f;   // two 128-row query tiles x 128 keys, head_dim 128, 16-bit
 constexpr float PF_STEP_CYCLES_D64 = 2700.f;    // the same at head_dim 64
-constexpr float PF_STEP_CYCLES_FP8 = 3900.f;    // head_dim 128 over an e4m3 cache (tiles widened first)
+constexpr float PF_STEP_CYCLES_FP8 = 3300.f;    // head_dim 128 over an e4m3 cache (tiles widened first)
 constexpr float PF_TILE_CYCLES = 1700.f;        // start and end of a work tile beyond its steps
 constexpr float DECODE_LATENCY_S = 2.3e-6f;     // loaded HBM latency of the decode kernel's TMA stream
 constexpr float HBM_STREAM_EFF = 0.83f;         // streamable fraction of the HBM pin rate (measured copy)

@@ -109,22 +109,13 @@ struct Cfg2 {
 // tcgen05.mma .kind::f16 with the A operand (M x K, 16-bit, packed in pairs per
 // 32-bit column, one row per lane) in TMEM and B in shared memory.
 // D[tmem] (+)= A[tmem] * B[smem], the warp-wide form of mma_f16_ss_warp.
-template <bool ELECT>
 __device__ __forceinline__ void mma_f16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                                 uint32_t accumulate) {
-  if constexpr (ELECT) {
-    asm volatile(
-        "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
-        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n .reg .pred p, e;\n .reg .u32 l;\n setp.ne.b32 p, %4, 0;\n mov.u32 l, %%laneid;\n"
-        " setp.eq.u32 e, l, 0;\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  }
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -169,27 +160,39 @@ __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t codes) {
 // reads all 128 codes of its row before writing it, so row r of the upper half
 // (its own codes) is overwritten only after it was read. Rows >= zero_from are
 // written as zeros (the V rows past the sequence's end: 0 * (NaN code) must not
-// reach O).
+// reach O), decided once per row: a select per converted pair instead made the
+// widening warps, which share SM sub-partitions with the softmax warps, cost the
+// chunks of the mixed tick 177 us against 155 us.
 __device__ __forceinline__ void widen_rows(unsigned char* slot, int r0, int r1, int lane, int zero_from) {
   const unsigned char* stg = slot + BN * 128;
   for (int r = r0 + lane; r < r1; r += 32) {
+    const int sw = r & 7;
+    if (r >= zero_from) {
+      // a V row past the sequence's end (only in the last tile): zeros
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        unsigned char* row = slot + (k >> 2) * BN * 128 + r * 128;
+        *reinterpret_cast<uint4*>(row + (((k & 3) * 2) ^ sw) * 16) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(row + ((((k & 3) * 2 + 1) ^ sw) * 16)) = make_uint4(0, 0, 0, 0);
+      }
+      continue;
+    }
     uint4 c[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) c[k] = *reinterpret_cast<const uint4*>(stg + r * 128 + ((k ^ (r & 7)) << 4));
-    const bool z = r >= zero_from;
+    for (int k = 0; k < 8; ++k) c[k] = *reinterpret_cast<const uint4*>(stg + r * 128 + ((k ^ sw) << 4));
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const uint32_t w[4] = {c[k].x, c[k].y, c[k].z, c[k].w};
       uint32_t h[8];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        h[2 * q] = z ? 0u : e4m3x2_to_h2(w[q]);
-        h[2 * q + 1] = z ? 0u : e4m3x2_to_h2(w[q] >> 16);
+        h[2 * q] = e4m3x2_to_h2(w[q]);
+        h[2 * q + 1] = e4m3x2_to_h2(w[q] >> 16);
       }
       unsigned char* row = slot + (k >> 2) * BN * 128 + r * 128;   // dims 16k..16k+15: half k / 4
       const int ch = (k & 3) * 2;
-      *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-      *reinterpret_cast<uint4*>(row + (((ch + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+      *reinterpret_cast<uint4*>(row + ((ch ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(row + (((ch + 1) ^ sw) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
     }
   }
 }
@@ -468,11 +471,7 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
     // MMA stream loses issue slots to the softmax warps of its SM
     // sub-partition: measured on GB300, a dense FMA stream in those warps
     // slowed back-to-back M128 N128 K16 MMAs from 64 to ~140 cycles each,
-    // against ~67 with the warp-uniform loop. fp8 caches keep lane 0 as the
-    // issuer: there the widening warps are the bound, and the elected issue
-    // took issue slots from them (the chunks of the mixed tick over an e4m3
-    // cache: 177 us with lane 0, 183 us elected).
-    constexpr bool ELECT = !KV8;
+    // against ~67 with the warp-uniform loop.
     // The tensor pipe holds only a few MMAs ahead of the issue, and each
     // barrier wait or commit here costs on the order of 100 cycles, so the
     // waits for the next operands sit behind MMAs already queued: K_j after
@@ -491,10 +490,10 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk / 4) * BM * 128 + (kk % 4) * 32;
         const uint32_t offk = (kk / 4) * BN * 128 + (kk % 4) * 32;
-        mma_f16_ss_warp<ELECT>(tmem + w * 128, qd + (uint64_t)((w * C::Q_BYTES + off) >> 4), kd + (uint64_t)(offk >> 4),
+        mma_f16_ss_warp(tmem + w * 128, qd + (uint64_t)((w * C::Q_BYTES + off) >> 4), kd + (uint64_t)(offk >> 4),
                          id_qk, kk > 0 ? 1u : 0u);
       }
-      mma_commit_warp<ELECT>(&bar_sfull[w]);
+      mma_commit_warp(&bar_sfull[w]);
     };
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       return warp_wait_or_abort(bar, parity, &s_abort, &p.ctrl[CTRL_ERR], p.dev_status);
@@ -521,8 +520,8 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
       if (ok) {
 #pragma unroll
         for (int w = 0; w < NWG; ++w) issue_qk(w, ks);
-        mma_commit_warp<ELECT>(&bar_empty[ks]);
-        if (ti.n_kv == 1) mma_commit_warp<ELECT>(&bar_qempty);
+        mma_commit_warp(&bar_empty[ks]);
+        if (ti.n_kv == 1) mma_commit_warp(&bar_qempty);
         ks += 2;
         if (ks >= (uint32_t)NS) {
           ks -= NS;
@@ -552,12 +551,12 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_f16_ts_warp<ELECT>(tmem + 256 + w * 128, tmem + w * 128 + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4),
+            mma_f16_ts_warp(tmem + 256 + w * 128, tmem + w * 128 + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4),
                              id_pv, kk > 0 ? 1u : acc0);
-          if (j == ti.n_kv) mma_commit_warp<ELECT>(&bar_odone[w]);
+          if (j == ti.n_kv) mma_commit_warp(&bar_odone[w]);
           if (w == NWG - 1) {
             // V_{j-1} has no reader left
-            mma_commit_warp<ELECT>(&bar_empty[vs]);
+            mma_commit_warp(&bar_empty[vs]);
             vs += 2;
             if (vs >= (uint32_t)NS) {
               vs -= NS;
@@ -578,8 +577,8 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
         }
         if (!ok) break;
         if (qk) {
-          mma_commit_warp<ELECT>(&bar_empty[kslot]);
-          if (j == ti.n_kv - 1) mma_commit_warp<ELECT>(&bar_qempty);
+          mma_commit_warp(&bar_empty[kslot]);
+          if (j == ti.n_kv - 1) mma_commit_warp(&bar_qempty);
           ks += 2;
           if (ks >= (uint32_t)NS) {
             ks -= NS;
@@ -763,7 +762,7 @@ __global__ void __launch_bounds__(KV8 ? NTHREADS_KV8 : NTHREADS, 1)
 
   if (warp == 1) {
     // every MMA this warp issued is complete before TMEM is released
-    mma_commit_warp<!KV8>(&bar_drain);
+    mma_commit_warp(&bar_drain);
     mbar_wait(&bar_drain, 0, 500000000ull);
     __syncwarp();
   }

@@ -204,44 +204,26 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// Warp-wide forms: the whole warp executes them with warp-uniform operands
-// and one lane issues. ELECT: elect.sync picks that lane (with every lane
-// active the same lane is elected each time, so a commit covers every MMA the
-// warp issued before it); otherwise lane 0 issues, chosen by its lane id.
-// The elected form keeps a single issuing thread's MMA stream at full rate
-// beside busy warps of the same SM sub-partition; the lane-id form gives
-// those warps more of the issue slots.
-template <bool ELECT>
+// Warp-wide forms: the whole warp executes them with warp-uniform operands and
+// elect.sync picks the lane that issues. With every lane active the same lane is
+// elected each time, so a commit covers every MMA the warp issued before it.
+// Issued this way, a single thread's MMA stream keeps its issue slots beside
+// busy warps of the same SM sub-partition (issued from one lane's divergent
+// code, or under a lane-id predicate, it does not).
 __device__ __forceinline__ void mma_f16_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                                 uint32_t accumulate) {
-  if constexpr (ELECT) {
-    asm volatile(
-        "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
-        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n .reg .pred p, e;\n .reg .u32 l;\n setp.ne.b32 p, %4, 0;\n mov.u32 l, %%laneid;\n"
-        " setp.eq.u32 e, l, 0;\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  }
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
-template <bool ELECT>
 __device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
-  if constexpr (ELECT) {
-    asm volatile(
-        "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
-        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(smem_u32(bar))
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n .reg .pred e;\n .reg .u32 l;\n mov.u32 l, %%laneid;\n setp.eq.u32 e, l, 0;\n"
-        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(smem_u32(bar))
-        : "memory");
-  }
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(smem_u32(bar))
+      : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets lane
