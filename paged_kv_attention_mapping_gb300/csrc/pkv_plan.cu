@@ -209,17 +209,18 @@ __device__ int prefill_ctas(const PlanArgs& a, int n_pairs, unsigned long long s
   const float bw_sm = a.dec_inflight_bytes / DECODE_LATENCY_S;
   const float hbm = a.hbm_bps * HBM_STREAM_EFF;
   const float r_all = fminf((float)N * bw_sm, hbm);
+  // the divisions are an estimate's: __fdividef is enough (and short)
   int best = N;
-  float best_t = pf / (float)N + dec / r_all;   // one after the other on every SM
+  float best_t = __fdividef(pf, (float)N) + __fdividef(dec, r_all);   // one after the other on every SM
   // Below about a third of the SMs the prefill kernel's steps run well over
   // their cycle count beside a decode kernel that saturates HBM (its operand
   // loads queue behind the decode stream; measured on ticks of 192 and 256
   // decode rows beside two chunks: 563 and 164 us with 40 prefill SMs against
   // 538 and 153 us with 52), so the search starts there.
   for (int x = (N + 2) / 3 + lane; x < N; x += 32) {
-    const float t_pf = pf / (float)x;
+    const float t_pf = __fdividef(pf, (float)x);
     const float r = fminf((float)(N - x) * bw_sm, hbm);
-    const float t = dec <= t_pf * r ? t_pf : t_pf + (dec - t_pf * r) / r_all;
+    const float t = dec <= t_pf * r ? t_pf : t_pf + __fdividef(dec - t_pf * r, r_all);
     if (t < best_t) {
       best_t = t;
       best = x;
@@ -493,8 +494,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
   }
   int pf_ctas = a.num_sms;
   if (tid < 32) {
-    unsigned long long steps = 0;
-    for (int k = 0; k < 32; ++k) steps += s_wsteps[k];
+    unsigned long long steps = s_wsteps[tid];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) steps += __shfl_xor_sync(0xffffffffu, steps, o);
     pf_ctas = prefill_ctas(a, n_pairs, steps, s_keys, tid);
   }
   if (tid == 0) {
