@@ -220,8 +220,11 @@ size_t pkv_paged_attention_workspace_size(int32_t num_seqs, int32_t total_q, int
  * Rows of sequences with bad lengths or pages (see the device status bits)
  * are skipped.
  * Errors: PKV_E_NULL, PKV_E_DTYPE, PKV_E_SHAPE (num_q_heads % num_kv_heads != 0,
- * a group num_q_heads / num_kv_heads outside 1..8 and 16, head_dim not 64 or
- * 128, sizes < 0), PKV_E_ALIGN, PKV_E_WORKSPACE, PKV_E_DEVICE, PKV_E_CUDA.
+ * a group num_q_heads / num_kv_heads outside 1..8 and 16, head_dim not 64,
+ * 128 or 256, sizes < 0), PKV_E_ALIGN, PKV_E_WORKSPACE, PKV_E_DEVICE, PKV_E_CUDA.
+ * head_dim 64 and 128 run decode rows on the TMA-staged decode kernel and
+ * chunks on the tensor-core prefill kernels; head_dim 256 runs every row on the
+ * CUDA-core rows kernel.
  */
 int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, const int32_t* kv_lens,
                         const int32_t* page_tables, int32_t num_seqs, int32_t total_q,

@@ -195,7 +195,9 @@ extern "C" int pkv_rope_kv_append(const void* q, const void* k, const void* v, c
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "rope_append");
 }
 
-static bool head_dim_supported(int d) { return d == 64 || d == 128; }
+// head_dim 64 and 128 run on the TMA decode and tcgen05 prefill kernels; 256
+// runs every row on the CUDA-core rows kernel
+static bool head_dim_supported(int d) { return d == 64 || d == 128 || d == 256; }
 // q heads per KV head the kernels are built for (1 to 8, and 16)
 static bool group_supported(int g) { return (g >= 1 && g <= 8) || g == 16; }
 

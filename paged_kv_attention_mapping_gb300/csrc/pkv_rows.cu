@@ -180,8 +180,9 @@ __global__ void __launch_bounds__(ROWS_WARPS * 32) rows_kernel(AttnArgs a) {
 // unrolled so several splits' loads are in flight at once.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) combine_kernel(AttnArgs a) {
-  constexpr int DPL = D / 32;
-  using V = typename std::conditional<DPL == 4, float4, float2>::type;
+  constexpr int DPL = D / 32;                       // 2, 4 or 8 dims per lane
+  using V = typename std::conditional<DPL == 2, float2, float4>::type;
+  constexpr int NV = DPL == 2 ? 1 : DPL / 4;        // vector loads per split and lane
   const int lane = threadIdx.x & 31;
   pdl_wait();   // launched to overlap the end of the decode kernel, whose partials it reads
   const int32_t* ctrl = (const int32_t*)(a.ws + a.lay.ctrl);
@@ -214,22 +215,25 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnArgs a) {
     const float gmx = warp_max(mx);
     sm = mx == -INFINITY ? 0.f : sm * __expf(mx - gmx);
     const float lse = gmx + __logf(warp_sum(sm));
-    V acc;
-    float* av = reinterpret_cast<float*>(&acc);
+    float av[DPL];
 #pragma unroll
     for (int c = 0; c < DPL; ++c) av[c] = 0.f;
     for (int s0 = 0; s0 < nsplit; s0 += 32) {
       const int n = min(32, nsplit - s0);
       const float wl = lane < n ? __expf(part_lse[(int64_t)(p0 + s0 + lane) * G + hh] - lse) : 0.f;
-      const V* src = reinterpret_cast<const V*>(part_o + ((int64_t)(p0 + s0) * G + hh) * D) + lane;
-      const int64_t stride = (int64_t)G * D / DPL;   // vectors between consecutive splits
+      const V* src = reinterpret_cast<const V*>(part_o + ((int64_t)(p0 + s0) * G + hh) * D) + lane * NV;
+      const int64_t stride = (int64_t)G * D * sizeof(float) / sizeof(V);   // vectors between consecutive splits
 #pragma unroll 4
       for (int j = 0; j < n; ++j) {
         const float wgt = __shfl_sync(0xffffffffu, wl, j);
-        const V x = __ldg(src + j * stride);
-        const float* xv = reinterpret_cast<const float*>(&x);
 #pragma unroll
-        for (int c = 0; c < DPL; ++c) av[c] = fmaf(wgt, xv[c], av[c]);
+        for (int q = 0; q < NV; ++q) {
+          const V x = __ldg(src + j * stride + q);
+          const float* xv = reinterpret_cast<const float*>(&x);
+#pragma unroll
+          for (int c = 0; c < (int)(sizeof(V) / sizeof(float)); ++c)
+            av[q * (int)(sizeof(V) / sizeof(float)) + c] = fmaf(wgt, xv[c], av[q * (int)(sizeof(V) / sizeof(float)) + c]);
+        }
       }
     }
     T* dst = (T*)a.out + ((int64_t)r * a.Hq + h) * D + lane * DPL;
@@ -241,7 +245,8 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnArgs a) {
 
 template <typename T, int D, int G>
 static cudaError_t launch_rows_g(const AttnArgs& a, cudaStream_t s) {
-  constexpr int U = G >= 8 ? 2 : 4;
+  // keys per step: fewer where a lane already holds many q and o values
+  constexpr int U = D >= 256 ? (G >= 4 ? 1 : 2) : (G >= 8 ? 2 : 4);
   const int blocks = a.num_sms * ROWS_BLOCKS_PER_SM;
   rows_kernel<T, D, G, U><<<blocks, ROWS_WARPS * 32, 0, s>>>(a);
   return cudaGetLastError();
@@ -265,7 +270,12 @@ static cudaError_t launch_rows_d(const AttnArgs& a, cudaStream_t s) {
 
 template <typename T>
 static cudaError_t launch_rows_t(const AttnArgs& a, cudaStream_t s) {
-  return a.D == 64 ? launch_rows_d<T, 64>(a, s) : launch_rows_d<T, 128>(a, s);
+  switch (a.D) {
+    case 64: return launch_rows_d<T, 64>(a, s);
+    case 128: return launch_rows_d<T, 128>(a, s);
+    case 256: return launch_rows_d<T, 256>(a, s);
+    default: return cudaErrorNotSupported;
+  }
 }
 
 cudaError_t launch_rows(const AttnArgs& a, cudaStream_t s) {
@@ -282,8 +292,13 @@ static cudaError_t launch_combine_t(const AttnArgs& a, cudaStream_t s) {
   const int blocks = a.num_sms * 2;
   // the grid may get resident once the decode kernel's CTAs have all started;
   // it waits for that grid to finish before reading the partials
-  const cudaError_t e = a.D == 64 ? launch_after_trigger(combine_kernel<T, 64>, dim3(blocks), dim3(256), 0, s, a)
-                                  : launch_after_trigger(combine_kernel<T, 128>, dim3(blocks), dim3(256), 0, s, a);
+  cudaError_t e = cudaErrorNotSupported;
+  switch (a.D) {
+    case 64: e = launch_after_trigger(combine_kernel<T, 64>, dim3(blocks), dim3(256), 0, s, a); break;
+    case 128: e = launch_after_trigger(combine_kernel<T, 128>, dim3(blocks), dim3(256), 0, s, a); break;
+    case 256: e = launch_after_trigger(combine_kernel<T, 256>, dim3(blocks), dim3(256), 0, s, a); break;
+    default: break;
+  }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -160,11 +160,11 @@ def test_workspace_size(lib):
 
 
 def test_attention_rejects_unsupported_shapes_on_the_host(lib):
-    """Group sizes outside 1..8 and 16, and head_dim outside {64, 128}, are
-    refused before any device work (PKV_E_SHAPE)."""
+    """Group sizes outside 1..8 and 16, and head_dim outside {64, 128, 256}, are
+    refused before any device work (PKV_E_SHAPE); an fp8 cache needs head_dim 128."""
     import ctypes
     fake = ctypes.c_void_p(256)
-    for heads, kv_heads, d in ((40, 4, 128), (32, 8, 96), (36, 3, 128), (24, 1, 64)):
+    for heads, kv_heads, d in ((40, 4, 128), (32, 8, 96), (36, 3, 128), (24, 1, 64), (8, 2, 192), (8, 2, 512)):
         desc = binding.CacheDesc(4, 16, kv_heads, d, binding.PKV_BF16)
         st = lib.pkv_paged_attention(fake, fake, fake, fake, 1, 1, heads, 1, 16, fake, fake, ctypes.byref(desc),
                                      ctypes.c_float(1.0), fake, None, fake, 1 << 20, None)
@@ -172,6 +172,21 @@ def test_attention_rejects_unsupported_shapes_on_the_host(lib):
         st = lib.pkv_paged_attention_no_alloc(fake, fake, fake, fake, 1, 1, heads, 1, 16, fake, fake,
                                               ctypes.byref(desc), ctypes.c_float(1.0), fake, None, None)
         assert st == -3, (heads, kv_heads, d, st)
+
+
+def test_head_dim_256_is_accepted_on_the_host(lib):
+    """head_dim 256 (every row on the CUDA-core rows kernel) gets a workspace
+    size; an e4m3 cache at 256 is refused."""
+    import ctypes
+    desc = binding.CacheDesc(4, 16, 2, 256, binding.PKV_BF16)
+    n = lib.pkv_paged_attention_workspace_size(4, 10, 8, ctypes.byref(desc), 512)
+    assert n > 0 and n % 256 == 0
+    fake = ctypes.c_void_p(256)
+    fp8 = binding.CacheDesc(4, 16, 2, 256, binding.PKV_FP8_E4M3)
+    scale = ctypes.c_float(1.0)
+    st = lib.pkv_paged_attention_fp8(fake, binding.PKV_BF16, fake, fake, fake, 1, 1, 8, 1, 16, fake, fake,
+                                     ctypes.byref(fp8), fake, fake, scale, fake, None, fake, 1 << 20, None)
+    assert st == -3
 
 
 def test_no_alloc_rejects_oversized_plans_on_the_host(lib):
