@@ -223,8 +223,9 @@ size_t pkv_paged_attention_workspace_size(int32_t num_seqs, int32_t total_q, int
  * a group num_q_heads / num_kv_heads outside 1..8 and 16, head_dim not 64,
  * 128 or 256, sizes < 0), PKV_E_ALIGN, PKV_E_WORKSPACE, PKV_E_DEVICE, PKV_E_CUDA.
  * head_dim 64 and 128 run decode rows on the TMA-staged decode kernel and
- * chunks on the tensor-core prefill kernels; head_dim 256 runs every row on the
- * CUDA-core rows kernel.
+ * chunks on the tensor-core prefill kernels; at head_dim 256 every row (decode
+ * and chunk) runs on the TMA-staged decode kernel over 16-bit caches and on the
+ * CUDA-core rows kernel over fp32 caches.
  */
 int pkv_paged_attention(const void* q, const int32_t* cu_seqlens_q, const int32_t* kv_lens,
                         const int32_t* page_tables, int32_t num_seqs, int32_t total_q,

@@ -28,11 +28,12 @@ int inflight_g(int group) {
 int decode_inflight_bytes(int kv_dtype, int D, int group) {
   if (kv_dtype == PKV_FP8_E4M3) return D == 128 ? inflight_g<uint8_t, 128>(group) : 0;
   if (kv_dtype == PKV_F32) return D == 64 ? inflight_g<float, 64>(group) : inflight_g<float, 128>(group);
+  if (D == 256) return inflight_g<__half, 256>(group);
   return D == 64 ? inflight_g<__half, 64>(group) : inflight_g<__half, 128>(group);
 }
 
 bool decode_supported(int dtype, int D, int P) {
-  if (D != 64 && D != 128) return false;
+  if (D != 64 && D != 128 && !(D == 256 && (dtype == PKV_F16 || dtype == PKV_BF16))) return false;
   if (dtype == PKV_FP8_E4M3 && D != 128) return false;   // fp8 rows must fill a 128-byte swizzle atom
   if (P % BT == 0) return true;
   return P >= 8 && P % 8 == 0 && BT % P == 0;

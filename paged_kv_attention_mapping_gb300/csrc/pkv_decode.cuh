@@ -210,8 +210,11 @@ struct DCfg {
   // head_dim 64) get as many as fit two CTAs per SM, up to 6.
   // CTAs per SM: small stages (head_dim 64 at 16 bits, fp8) run CPS_SMALL CTAs
   // so that more producers stream at once (a CTA's TMA boxes are processed in
-  // order, so each CTA's stream has a fixed rate); the rest run 2.
-  static constexpr int CPS = (STAGE_BYTES <= 16384 && ELT <= 2 && G <= 8) ? PKV_DEC_CPS_SMALL : 2;
+  // order, so each CTA's stream has a fixed rate); 64 KB stages (head_dim 256)
+  // run one CTA with three of them; the rest run 2.
+  static constexpr int CPS = (STAGE_BYTES <= 16384 && ELT <= 2 && G <= 8) ? PKV_DEC_CPS_SMALL
+                             : STAGE_BYTES > 32768                         ? 1
+                                                                           : 2;
   static constexpr int BASE_NST = STAGE_BYTES <= 32768 ? 3 : 2;
   // 228 KB of shared memory per SM, 1 KB of it reserved per CTA, ~0.5 KB static
   static constexpr int nst_for(int merge_smem) {
@@ -1077,6 +1080,9 @@ cudaError_t launch_dec_g(const AttnArgs& a, cudaStream_t s) {
 
 template <typename T>
 cudaError_t launch_dec_d(const AttnArgs& a, cudaStream_t s) {
+  if constexpr (sizeof(T) == 2) {
+    if (a.D == 256) return launch_dec_g<T, T, 256>(a, s);   // 16-bit caches only: 64 KB stages
+  }
   return a.D == 64 ? launch_dec_g<T, T, 64>(a, s) : launch_dec_g<T, T, 128>(a, s);
 }
 

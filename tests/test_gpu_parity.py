@@ -131,8 +131,9 @@ RAGGED = [
     (53, 5, 12, 2, 64, 16, "f16", (1, 3, 100), 900),      # g = 6, two query tiles per CTA
     (54, 4, 28, 4, 128, 64, "f16", (1, 130), 2300),       # g = 7
     (55, 6, 21, 7, 64, 32, "f32", (1, 5), 1300),          # g = 3 over an fp32 cache
-    # head_dim 256: every row (decode and chunk) on the CUDA-core rows kernel,
-    # rows past 2048 keys split and merged by the combine kernel
+    # head_dim 256: every row (decode and chunk) on the TMA decode kernel over
+    # 16-bit caches and the CUDA-core rows kernel over fp32 caches, rows past
+    # 2048 keys split and merged by the combine kernel
     (61, 4, 16, 4, 256, 16, "bf16", (1, 2, 70), 2600),    # g = 4, splits
     (62, 3, 8, 8, 256, 64, "f16", (1, 130), 900),         # g = 1, a chunk of 130 rows
     (63, 3, 8, 1, 256, 32, "f32", (1, 3), 2500),          # g = 8 over an fp32 cache, splits
