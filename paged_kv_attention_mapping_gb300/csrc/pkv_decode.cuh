@@ -211,7 +211,8 @@ struct DCfg {
   // CTAs per SM: small stages (head_dim 64 at 16 bits, fp8) run CPS_SMALL CTAs
   // so that more producers stream at once (a CTA's TMA boxes are processed in
   // order, so each CTA's stream has a fixed rate); 64 KB stages (head_dim 256)
-  // run one CTA with three of them; the rest run 2.
+  // run one CTA (with three stages up to 6 q heads per KV head, two above);
+  // the rest run 2.
   static constexpr int CPS = (STAGE_BYTES <= 16384 && ELT <= 2 && G <= 8) ? PKV_DEC_CPS_SMALL
                              : STAGE_BYTES > 32768                         ? 1
                                                                            : 2;
