@@ -74,6 +74,8 @@ cudaError_t launch_append(const void* k, const void* v, const int64_t* slots, in
   const int elt = c.dtype == PKV_F32 ? 4 : 2;
   const int32_t row_vecs = (int32_t)((int64_t)c.num_kv_heads * c.head_dim * elt / 16);
   const TokenSpan sp = token_span(T, 2 * row_vecs, num_sms, APPEND_U);
+  static const cudaError_t carve = prefer_max_shared(kv_append_kernel);
+  if (carve != cudaSuccess) return carve;
   KernelTimer timer("kv_append", s);
   kv_append_kernel<<<(unsigned)sp.blocks(), APPEND_THREADS, 0, s>>>(
       (const uint4*)k, (const uint4*)v, slots, sp, row_vecs, (int64_t)c.num_pages * c.page_size, (uint4*)kc,
@@ -143,6 +145,13 @@ cudaError_t launch_append_quant(const void* k, const void* v, int src_dtype, con
   const TokenSpan sp = token_span(T, 2 * row_vecs, num_sms, 2);
   const unsigned blocks = (unsigned)sp.blocks();
   const int64_t pool_slots = (int64_t)c.num_pages * c.page_size;
+  static const cudaError_t carve = [] {
+    cudaError_t e = prefer_max_shared(kv_append_quant_kernel<float>);
+    if (e == cudaSuccess) e = prefer_max_shared(kv_append_quant_kernel<__half>);
+    if (e == cudaSuccess) e = prefer_max_shared(kv_append_quant_kernel<__nv_bfloat16>);
+    return e;
+  }();
+  if (carve != cudaSuccess) return carve;
   KernelTimer timer("kv_append_quant", s);
   switch (src_dtype) {
     case PKV_F32:

@@ -98,6 +98,18 @@ struct PlanArgs {
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s);
 
+// Prefer the largest shared-memory carveout for a kernel that itself needs
+// little or none (the appends, the plan, the combine). Their blocks then leave
+// the SM configured as the kernels launched next need it: a CTA that needs more
+// shared memory than an SM's current carveout gives waits until that SM has
+// drained, which kept the plan kernel (12 KB) from starting beside the append
+// blocks. Called once per kernel (a function-local static at its launch site).
+template <typename K>
+cudaError_t prefer_max_shared(K kernel) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared);
+}
+
 // Launch with programmatic stream serialization: the kernel may start as soon
 // as the preceding kernel of the stream calls pdl_trigger() (or completes).
 template <typename... KArgs, typename... Args>
@@ -152,17 +164,23 @@ struct AttnArgs {
 // takes tokens [b * tpb, (b + 1) * tpb) and its 256 threads take the items of
 // that span in order, so consecutive threads touch consecutive 16-byte vectors
 // of one token's rows (coalesced reads and writes). tpb is chosen so that a
-// thread has at most about four items and the grid has at least two blocks per
-// SM when the tick has enough tokens.
+// thread has about items_per_thread items a pass and the grid has at least two
+// blocks per SM when the tick has enough tokens, but at most three: the blocks
+// then loop over their span, and the attention call's plan kernel, launched
+// next, finds room beside them (with six append blocks on every SM it waited
+// for the first SM to drain, ~5 us on the mixed tick).
 struct TokenSpan {
   int32_t T, per_token, tpb;
   int64_t blocks() const { return ((int64_t)T + tpb - 1) / tpb; }
 };
 inline TokenSpan token_span(int32_t T, int32_t per_token, int num_sms, int items_per_thread) {
+  const int n = num_sms > 0 ? num_sms : 1;
   int32_t tpb = (256 * items_per_thread) / per_token;
   if (tpb < 1) tpb = 1;
-  const int32_t for_grid = T / (2 * (num_sms > 0 ? num_sms : 1));   // tokens per block with 2 blocks per SM
+  const int32_t for_grid = T / (2 * n);   // tokens per block with 2 blocks per SM
   if (for_grid < tpb) tpb = for_grid < 1 ? 1 : for_grid;
+  const int32_t min_tpb = (int32_t)(((int64_t)T + 3 * n - 1) / (3 * n));   // at most 3 blocks per SM
+  if (tpb < min_tpb) tpb = min_tpb;
   return TokenSpan{T, per_token, tpb};
 }
 

@@ -71,7 +71,14 @@ __device__ __forceinline__ int upper_bound_written(const volatile int32_t* a, in
   return lo;
 }
 
-// Exclusive scan over the 1024 threads of the block; *total gets the sum.
+// Threads of the plan's one CTA. 512 (28.7K registers) lets it start on an
+// SM beside the append kernel's blocks (at most three per SM), which it may
+// overlap; 1024 needed an SM with no append block left and started ~5 us later
+// on the mixed tick.
+constexpr int PLAN_THREADS = 512;
+constexpr int PLAN_WARPS = PLAN_THREADS / 32;
+
+// Exclusive scan over the threads of the block; *total gets the sum.
 __device__ int block_scan_excl(int v, int* total, int* sm) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   int x = v;
@@ -83,7 +90,7 @@ __device__ int block_scan_excl(int v, int* total, int* sm) {
   if (lane == 31) sm[w] = x;
   __syncthreads();
   if (w == 0) {
-    int s = sm[lane];
+    int s = lane < PLAN_WARPS ? sm[lane] : 0;   // the lanes past the last warp hold the total
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, s, o);
@@ -98,7 +105,7 @@ __device__ int block_scan_excl(int v, int* total, int* sm) {
   return res;
 }
 
-// Exclusive scan of N values at once over the 1024 threads of the block.
+// Exclusive scan of N values at once over the threads of the block.
 template <int N>
 __device__ void block_scan_n(const int (&v)[N], int (&ex)[N], int (&tot)[N], int (*sm)[32]) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -121,7 +128,7 @@ __device__ void block_scan_n(const int (&v)[N], int (&ex)[N], int (&tot)[N], int
   if (w == 0) {
 #pragma unroll
     for (int k = 0; k < N; ++k) {
-      int s = sm[k][lane];
+      int s = lane < PLAN_WARPS ? sm[k][lane] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, s, o);
@@ -243,7 +250,7 @@ __device__ int prefill_ctas(const PlanArgs& a, int n_pairs, unsigned long long s
 constexpr int PLAN_SMEM_SEQS = 6144;
 constexpr int PLAN_SMEM_WORDS = (3 + SEQ_OFFS) * PLAN_SMEM_SEQS + 2;
 
-__global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_status) {
+__global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(PlanArgs a_in, int32_t* dev_status) {
   // stage cu_seqlens_q and kv_lens in shared memory: every row below searches them
   extern __shared__ int32_t s_seq[];
   // A decode kernel launched next may get resident now (it waits for this
@@ -313,7 +320,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
     if (my_err) atomicOr(&s_err, my_err);
   }
   const bool any_tc = __syncthreads_or(my_tc) != 0;   // no prefill-kernel sequence: skip pass 3
-  unsigned long long s_keys = s_wkeys[tid & 31];
+  unsigned long long s_keys = (tid & 31) < PLAN_WARPS ? s_wkeys[tid & 31] : 0ull;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s_keys += __shfl_xor_sync(0xffffffffu, s_keys, o);
   // split size: about target_items items, at least chunk_min keys, multiple of 64
@@ -468,7 +475,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
     __syncthreads();
     // descending exclusive offsets: hist[w] <- number of pairs with work > w
     {
-      constexpr int PER = HIST / 1024;
+      constexpr int PER = HIST / PLAN_THREADS;
       int vals[PER], sum = 0;
   #pragma unroll
       for (int k = 0; k < PER; ++k) {
@@ -494,7 +501,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a_in, int32_t* dev_
   }
   int pf_ctas = a.num_sms;
   if (tid < 32) {
-    unsigned long long steps = s_wsteps[tid];
+    unsigned long long steps = tid < PLAN_WARPS ? s_wsteps[tid] : 0ull;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) steps += __shfl_xor_sync(0xffffffffu, steps, o);
     pf_ctas = prefill_ctas(a, n_pairs, steps, s_keys, tid);
@@ -523,10 +530,12 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
   static cudaError_t attr = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  PLAN_SMEM_WORDS * 4);
   if (attr != cudaSuccess) return attr;
+  static const cudaError_t carve = prefer_max_shared(plan_kernel);
+  if (carve != cudaSuccess) return carve;
   const size_t smem = a.B <= PLAN_SMEM_SEQS ? (size_t)((3 + SEQ_OFFS) * a.B + 2) * 4 : 0;
   KernelTimer timer("plan", s);
   // may overlap the preceding append, which it does not read (see pdl_wait above)
-  cudaError_t e = launch_after_trigger(plan_kernel, dim3(1), dim3(1024), smem, s, a, a.dev_status);
+  cudaError_t e = launch_after_trigger(plan_kernel, dim3(1), dim3(PLAN_THREADS), smem, s, a, a.dev_status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -104,6 +104,13 @@ cudaError_t launch_rope_append(const void* q, const void* k, const void* v, cons
   const TokenSpan sp = token_span(T, per_token, num_sms, 2);
   const unsigned blocks = (unsigned)sp.blocks();
   const int64_t pool_slots = (int64_t)c.num_pages * c.page_size;
+  static const cudaError_t carve = [] {
+    cudaError_t e = prefer_max_shared(rope_append_kernel<float>);
+    if (e == cudaSuccess) e = prefer_max_shared(rope_append_kernel<__half>);
+    if (e == cudaSuccess) e = prefer_max_shared(rope_append_kernel<__nv_bfloat16>);
+    return e;
+  }();
+  if (carve != cudaSuccess) return carve;
   KernelTimer timer("rope_append", s);
   switch (c.dtype) {
     case PKV_F32:

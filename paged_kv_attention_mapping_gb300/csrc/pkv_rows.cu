@@ -290,6 +290,13 @@ cudaError_t launch_rows(const AttnArgs& a, cudaStream_t s) {
 template <typename T>
 static cudaError_t launch_combine_t(const AttnArgs& a, cudaStream_t s) {
   const int blocks = a.num_sms * 2;
+  static const cudaError_t carve = [] {
+    cudaError_t e = prefer_max_shared(combine_kernel<T, 64>);
+    if (e == cudaSuccess) e = prefer_max_shared(combine_kernel<T, 128>);
+    if (e == cudaSuccess) e = prefer_max_shared(combine_kernel<T, 256>);
+    return e;
+  }();
+  if (carve != cudaSuccess) return carve;
   // the grid may get resident once the decode kernel's CTAs have all started;
   // it waits for that grid to finish before reading the partials
   cudaError_t e = cudaErrorNotSupported;
