@@ -73,7 +73,7 @@ cudaError_t launch_append(const void* k, const void* v, const int64_t* slots, in
   if (T == 0) return cudaSuccess;
   const int elt = c.dtype == PKV_F32 ? 4 : 2;
   const int32_t row_vecs = (int32_t)((int64_t)c.num_kv_heads * c.head_dim * elt / 16);
-  const TokenSpan sp = token_span(T, 2 * row_vecs, num_sms, APPEND_U);
+  const TokenSpan sp = token_span(T, 2 * row_vecs, num_sms, APPEND_U, 3);
   static const cudaError_t carve = prefer_max_shared(kv_append_kernel);
   if (carve != cudaSuccess) return carve;
   KernelTimer timer("kv_append", s);

@@ -165,22 +165,28 @@ struct AttnArgs {
 // that span in order, so consecutive threads touch consecutive 16-byte vectors
 // of one token's rows (coalesced reads and writes). tpb is chosen so that a
 // thread has about items_per_thread items a pass and the grid has at least two
-// blocks per SM when the tick has enough tokens, but at most three: the blocks
-// then loop over their span, and the attention call's plan kernel, launched
-// next, finds room beside them (with six append blocks on every SM it waited
-// for the first SM to drain, ~5 us on the mixed tick).
+// blocks per SM when the tick has enough tokens. With max_per_sm > 0 the grid
+// also holds at most that many blocks per SM (the blocks then loop over their
+// span): the plain append uses three, so that the attention call's plan kernel,
+// launched next, finds room beside them (with six append blocks on every SM it
+// waited for the first SM to drain, ~5 us on the mixed tick). The quantising and
+// RoPE appends take one item per thread per iteration, load then store, so more
+// iterations would serialise their latency; they keep the one-pass grid.
 struct TokenSpan {
   int32_t T, per_token, tpb;
   int64_t blocks() const { return ((int64_t)T + tpb - 1) / tpb; }
 };
-inline TokenSpan token_span(int32_t T, int32_t per_token, int num_sms, int items_per_thread) {
+inline TokenSpan token_span(int32_t T, int32_t per_token, int num_sms, int items_per_thread, int max_per_sm = 0) {
   const int n = num_sms > 0 ? num_sms : 1;
   int32_t tpb = (256 * items_per_thread) / per_token;
   if (tpb < 1) tpb = 1;
   const int32_t for_grid = T / (2 * n);   // tokens per block with 2 blocks per SM
   if (for_grid < tpb) tpb = for_grid < 1 ? 1 : for_grid;
-  const int32_t min_tpb = (int32_t)(((int64_t)T + 3 * n - 1) / (3 * n));   // at most 3 blocks per SM
-  if (tpb < min_tpb) tpb = min_tpb;
+  if (max_per_sm > 0) {
+    const int64_t cap = (int64_t)max_per_sm * n;
+    const int32_t min_tpb = (int32_t)(((int64_t)T + cap - 1) / cap);
+    if (tpb < min_tpb) tpb = min_tpb;
+  }
   return TokenSpan{T, per_token, tpb};
 }
 
