@@ -513,3 +513,13 @@ def test_full_size_mixed_tick_odd_groups(dev, hq, hkv):
     finally:
         binding.set_kernel_timing(False)
     assert "prefill_tc" in launched and "decode" in launched, launched
+
+
+def test_more_than_256_prefill_tiles(dev):
+    """300 sequences of one 64-row chunk each (prefixes of 0-256 keys, head_dim 64,
+    pages of 16, group 4): 300 (sequence, q tile) pairs, more than the plan ranks
+    directly, so its counting sort orders the prefill kernel's tiles. Every chunk
+    is in the checked sub-problem; a few rows of each are compared."""
+    w = W.random_workload(71, 300, 8, 2, 64, 16, "bf16", (64,), 320)
+    assert sum(r.q_len for r in w.requests) == 300 * 64
+    full_size_check(w, dev, n_decode=0, chunk_rows=6, seed=3)
