@@ -301,7 +301,6 @@ int pkv::attention_impl(const void* q, int q_dtype, const int32_t* cu_seqlens_q,
   // it is packed into. It only grows when the partial results would overflow
   // the workspace.
   pa.chunk_min = split_chunk_keys(cache->head_dim, elt_bytes(cache->dtype));
-  pa.target_items = 1 << 30;
   pa.tc_min_q = tc ? TC_MIN_Q : 0;
   pa.num_sms = f->num_sms;
   pa.sm_hz = f->sm_hz;

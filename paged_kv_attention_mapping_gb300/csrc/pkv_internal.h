@@ -78,8 +78,7 @@ struct PlanArgs {
   const int32_t* kv_lens;  // [B]
   int32_t B, T, Hq, Hkv;
   int32_t max_kv_len, table_cap;  // table_cap = max_pages_per_seq * page_size
-  int32_t chunk_min;              // smallest split, keys (multiple of 64)
-  int32_t target_items;           // aim for about this many row-path items
+  int32_t chunk_min;              // split, keys (a power of two >= 64; doubled only when partials overflow)
   int32_t tc_min_q;               // sequences with q_len >= this use the prefill kernel; 0 = never
   int32_t num_sms;                // SMs of the device
   float sm_hz, hbm_bps;           // SM clock and HBM pin rate of the device (bytes / s)
@@ -133,6 +132,7 @@ cudaError_t launch_after_trigger(void (*kernel)(KArgs...), dim3 grid, dim3 block
 // head_dim 128 (1 MB of bf16 K+V, 512 KB of fp8) and 512 at 64, where ticks of
 // short contexts otherwise leave most SMs idle behind the longest rows
 // (measured on the TinyLlama- and Qwen3-shaped decode ticks, 16-bit and fp8).
+// Powers of two: the plan divides by the split size with shifts.
 inline int32_t split_chunk_keys(int head_dim, int /*elt*/) { return head_dim >= 128 ? 2048 : 512; }
 
 // ---------------------------------------------------------------------------

@@ -8,9 +8,11 @@
 //  * the list of rows that need a combine;
 //  * the (sequence, 128-row q tile) pairs of the tensor-core prefill kernel,
 //    sorted by descending KV-tile count so that long tiles start first.
-// The split size is chosen so that the row-path items number about
-// `target_items` (a few per resident worker), never below `chunk_min` keys,
-// and doubled until the partial results fit the workspace.
+// The split size is `chunk_min` keys (a power of two that depends only on
+// head_dim, so a row's result does not depend on the batch it is packed in),
+// doubled until the partial results fit the workspace, and at most the
+// smallest power of two that holds max_kv_len (one split a row). Being a power
+// of two, the closed forms below divide by it with shifts.
 #include <cuda_runtime.h>
 
 #include "pkv_common.cuh"
@@ -168,11 +170,11 @@ __device__ __forceinline__ SeqInfo seq_info(const PlanArgs& a, int b, bool parti
   return s;
 }
 
-// Sum of ceil(k / C) over k = 1 .. K (K >= 0): with K = m C + r, the first m C
-// terms give C (1 + .. + m) and the last r terms m + 1 each.
-__device__ __forceinline__ long long ceil_div_prefix(unsigned K, unsigned C) {
-  const unsigned m = K / C, r = K - m * C;
-  return (long long)C * m * (m + 1) / 2 + (long long)r * (m + 1);
+// Sum of ceil(k / C) over k = 1 .. K (K >= 0) for C = 2^s: with K = m C + r,
+// the first m C terms give C (1 + .. + m) and the last r terms m + 1 each.
+__device__ __forceinline__ long long ceil_div_prefix(unsigned K, int s) {
+  const unsigned m = K >> s, r = K & ((1u << s) - 1u);
+  return ((long long)m * (m + 1) / 2 << s) + (long long)r * (m + 1);
 }
 
 // How many SMs the prefill kernel keeps when the decode kernel can start on
@@ -323,14 +325,13 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(PlanArgs a_in, int32
   unsigned long long s_keys = (tid & 31) < PLAN_WARPS ? s_wkeys[tid & 31] : 0ull;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s_keys += __shfl_xor_sync(0xffffffffu, s_keys, o);
-  // split size: about target_items items, at least chunk_min keys, multiple of 64
-  const long long work = (long long)s_keys * Hkv;
-  long long C = (work + a.target_items - 1) / a.target_items;
-  if (C < a.chunk_min) C = a.chunk_min;
-  C = (C + 63) / 64 * 64;
-  const long long c_max = ((long long)a.max_kv_len + 63) / 64 * 64;
-  if (C > c_max) C = c_max;
-  if (C < 64) C = 64;
+  // split size C = 2^c_shift keys: chunk_min (a power of two), at most the
+  // smallest power of two >= max_kv_len (any C from there on gives one split a
+  // row)
+  int c_max_shift = 6;
+  while (c_max_shift < 31 && (1u << c_max_shift) < (unsigned)a.max_kv_len) ++c_max_shift;
+  int c_shift = 31 - __clz(a.chunk_min);
+  if (c_shift > c_max_shift) c_shift = c_max_shift;
 
   // pass 2a: per sequence, in closed form, its row-path rows, items and
   // partial slots, turned into offsets by a block scan. Row i of a row-path
@@ -340,7 +341,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(PlanArgs a_in, int32
   for (int guard = 0; guard < 40; ++guard) {
 #pragma unroll
     for (int k = 0; k < SEQ_OFFS; ++k) carry[k] = 0;
-    const unsigned Cu = (unsigned)C;
+    const unsigned Cu = 1u << c_shift;
     for (int base = 0; base < B; base += blockDim.x) {
       const int b = base + tid;
       int cnt[SEQ_OFFS] = {0, 0, 0, 0}, ex[SEQ_OFFS], tot[SEQ_OFFS];
@@ -354,12 +355,12 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(PlanArgs a_in, int32
             for (int off = 0; off < bytes; off += 128) prefetch_l2(t0 + off);
           }
           const unsigned k_lo = (unsigned)(s.L - s.q + 1), k_hi = (unsigned)s.L;
-          const long long f_hi = ceil_div_prefix(k_hi, Cu);
+          const long long f_hi = ceil_div_prefix(k_hi, c_shift);
           cnt[0] = s.q;
-          cnt[1] = (int)(f_hi - ceil_div_prefix(k_lo - 1, Cu)) * Hkv;
+          cnt[1] = (int)(f_hi - ceil_div_prefix(k_lo - 1, c_shift)) * Hkv;
           const unsigned k_s = k_lo > Cu + 1 ? k_lo : Cu + 1;   // first split row's key count
           if (k_hi >= k_s) {
-            cnt[2] = (int)(f_hi - ceil_div_prefix(k_s - 1, Cu)) * Hkv;
+            cnt[2] = (int)(f_hi - ceil_div_prefix(k_s - 1, c_shift)) * Hkv;
             cnt[3] = (int)(k_hi - k_s + 1);
           }
         }
@@ -372,8 +373,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(PlanArgs a_in, int32
 #pragma unroll
       for (int k = 0; k < SEQ_OFFS; ++k) carry[k] += tot[k];
     }
-    if (carry[2] <= a.lay.partial_cap || C >= c_max) break;
-    C = C * 2 < c_max ? C * 2 : c_max;   // grow the split until the partials fit
+    if (carry[2] <= a.lay.partial_cap || c_shift >= c_max_shift) break;
+    ++c_shift;   // grow the split until the partials fit
   }
   __syncthreads();   // seq_off complete
   const int n_rp = carry[0], n_items = carry[1], carry_parts = carry[2], carry_split = carry[3];
@@ -383,7 +384,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(PlanArgs a_in, int32
   // sequences share their successor's offset, so the last sequence whose offset
   // is <= j owns j), then its arrays from the same closed forms
   {
-    const unsigned Cu = (unsigned)C;
+    const unsigned Cu = 1u << c_shift;
     for (int j = tid; j < n_rp; j += blockDim.x) {
       int lo = 0, hi = B;   // first b with seq_off[SEQ_OFFS * b] > j
       while (lo < hi) {
@@ -398,11 +399,11 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(PlanArgs a_in, int32
       rp_seq[j] = b;
       rp_keys[j] = (int)k;
       rp_item_begin[j] = seq_off[SEQ_OFFS * b + 1] +
-                         (int)(ceil_div_prefix(k - 1, Cu) - ceil_div_prefix(k_lo - 1, Cu)) * Hkv;
+                         (int)(ceil_div_prefix(k - 1, c_shift) - ceil_div_prefix(k_lo - 1, c_shift)) * Hkv;
       int pb = -1;
       if (k > Cu) {
         const unsigned k_s = k_lo > Cu + 1 ? k_lo : Cu + 1;
-        pb = seq_off[SEQ_OFFS * b + 2] + (int)(ceil_div_prefix(k - 1, Cu) - ceil_div_prefix(k_s - 1, Cu)) * Hkv;
+        pb = seq_off[SEQ_OFFS * b + 2] + (int)(ceil_div_prefix(k - 1, c_shift) - ceil_div_prefix(k_s - 1, c_shift)) * Hkv;
         split_rows[seq_off[SEQ_OFFS * b + 3] + (int)(k - k_s)] = j;
       }
       rp_part_begin[j] = pb;
@@ -515,7 +516,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(PlanArgs a_in, int32
     ctrl[CTRL_N_PAIRS] = n_pairs;
     ctrl[CTRL_N_TILES] = n_pairs * a.Hq;
     ctrl[CTRL_TILE_NEXT] = 0;
-    ctrl[CTRL_CHUNK] = (int)C;
+    ctrl[CTRL_CHUNK] = (int)(1u << c_shift);
     ctrl[CTRL_N_SPLIT_ROWS] = carry_split;
     ctrl[CTRL_N_PARTIALS] = carry_parts;
     if (s_err) atomicOr(dev_status, s_err);
