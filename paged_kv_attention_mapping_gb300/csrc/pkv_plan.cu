@@ -73,8 +73,8 @@ __device__ __forceinline__ int upper_bound_written(const volatile int32_t* a, in
   return lo;
 }
 
-// Threads of the plan's one CTA. 512 (28.7K registers) lets it start on an
-// SM beside the append kernel's blocks (at most three per SM), which it may
+// Threads of the plan's one CTA. 512 (~33K registers) lets it start on an SM
+// beside the append kernel's blocks (at most three per SM, ~31K), which it may
 // overlap; 1024 needed an SM with no append block left and started ~5 us later
 // on the mixed tick.
 constexpr int PLAN_THREADS = 512;
